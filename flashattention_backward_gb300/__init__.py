@@ -1,0 +1,251 @@
+"""GB300 (sm_103a) FlashAttention-2 backward: Python binding of libfa.
+
+The binding only marshals arguments (shapes, strides, raw device pointers,
+the current CUDA stream) into the C ABI of ``include/fa.h``; every step of
+the computation runs in the library's CUDA kernels.  PyTorch supplies device
+memory and streams.  There is no fallback: if ``libfa.so`` is missing or a
+call fails, an exception is raised.
+
+Entry points mirror the C names: :func:`fa_fwd`, :func:`fa_bwd_preprocess`,
+:func:`fa_bwd`, :func:`fa_convert_dq`, :func:`fa_backward`, plus
+:func:`attention_forward` / :func:`attention_backward`, which allocate their
+outputs with torch and call those.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "FaError",
+    "FaProblem",
+    "problem_for",
+    "fa_dq_accum_elems",
+    "fa_fwd",
+    "fa_bwd_preprocess",
+    "fa_bwd",
+    "fa_convert_dq",
+    "fa_backward",
+    "attention_forward",
+    "attention_backward",
+    "get_device_status",
+    "set_wait_limit_ns",
+    "selftest_wait_timeout",
+    "library_path",
+    "load_library",
+]
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_DEVICE = range(6)
+FA_BF16, FA_FP32 = 0, 1
+TILE_ROWS = 128
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+class FaProblem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32),
+        ("H", ctypes.c_int32),
+        ("N", ctypes.c_int32),
+        ("d", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("causal", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("stride_b", ctypes.c_int64),
+        ("stride_h", ctypes.c_int64),
+        ("stride_n", ctypes.c_int64),
+    ]
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return os.environ.get("FA_LIBRARY", _build.LIB)
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libfa.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfa.so not found at {path}: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(FaProblem)
+    vp, fp, st = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
+    lib.fa_dq_accum_elems.argtypes = [P]
+    lib.fa_dq_accum_elems.restype = ctypes.c_size_t
+    lib.fa_fwd.argtypes = [P, vp, vp, vp, vp, fp, vp]
+    lib.fa_bwd_preprocess.argtypes = [P, vp, vp, fp, fp, vp]
+    lib.fa_bwd.argtypes = [P, vp, vp, vp, vp, fp, fp, fp, vp, vp, vp]
+    lib.fa_convert_dq.argtypes = [P, fp, vp, vp]
+    lib.fa_backward.argtypes = [P, vp, vp, vp, vp, vp, fp, fp, fp, vp, vp, vp, vp]
+    for name in ("fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_convert_dq", "fa_backward"):
+        getattr(lib, name).restype = st
+    lib.fa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.fa_get_device_status.restype = st
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.fa_set_wait_limit_ns.restype = None
+    lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.fa_selftest_wait_timeout.restype = st
+    lib.fa_status_string.argtypes = [st]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = ctypes.c_int32
+    _LIB = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load_library().fa_status_string(int(code)).decode()
+    except Exception:  # pragma: no cover - only for messages
+        return "status"
+
+
+def _check(code: int, what: str) -> None:
+    if code != FA_OK:
+        raise FaError(code, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def problem_for(q: torch.Tensor, scale: float, causal: bool) -> FaProblem:
+    """Problem descriptor for [B, H, N, d] tensors laid out like ``q``."""
+    if q.dim() != 4:
+        raise ValueError("expected a [B, H, N, d] tensor")
+    if q.stride(3) != 1:
+        raise ValueError("the last dimension must be contiguous")
+    B, H, N, d = q.shape
+    return FaProblem(B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), 0,
+                     q.stride(0), q.stride(1), q.stride(2))
+
+
+def _same_layout(p: FaProblem, *ts: torch.Tensor) -> None:
+    for t in ts:
+        if t.shape != (p.B, p.H, p.N, p.d) or t.stride() != (p.stride_b, p.stride_h, p.stride_n, 1):
+            raise ValueError("all [B, H, N, d] tensors must share shape and strides")
+        if _dtype_code(t) != p.dtype:
+            raise ValueError("all [B, H, N, d] tensors must share the dtype")
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+
+
+def _rows(p: FaProblem, *ts: torch.Tensor) -> None:
+    for t in ts:
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != p.B * p.H * p.N or not t.is_cuda:
+            raise ValueError("L and D must be contiguous float32 CUDA tensors of B*H*N elements")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+def fa_dq_accum_elems(p: FaProblem) -> int:
+    return int(load_library().fa_dq_accum_elems(ctypes.byref(p)))
+
+
+def fa_fwd(p: FaProblem, q, k, v, o, L, stream=None) -> None:
+    _same_layout(p, q, k, v, o)
+    _rows(p, L)
+    _check(load_library().fa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), _stream(stream)),
+           "fa_fwd")
+
+
+def fa_bwd_preprocess(p: FaProblem, o, do, D, dq_accum, stream=None) -> None:
+    _same_layout(p, o, do)
+    _rows(p, D)
+    _accum(p, dq_accum)
+    _check(load_library().fa_bwd_preprocess(ctypes.byref(p), _ptr(o), _ptr(do), _ptr(D), _ptr(dq_accum),
+                                            _stream(stream)), "fa_bwd_preprocess")
+
+
+def _accum(p: FaProblem, acc: torch.Tensor) -> None:
+    if acc.dtype != torch.float32 or not acc.is_contiguous() or acc.numel() < fa_dq_accum_elems(p):
+        raise ValueError("dq_accum must be a contiguous float32 tensor of fa_dq_accum_elems() elements")
+
+
+def fa_bwd(p: FaProblem, q, k, v, do, L, D, dq_accum, dk, dv, stream=None) -> None:
+    _same_layout(p, q, k, v, do, dk, dv)
+    _rows(p, L, D)
+    _accum(p, dq_accum)
+    _check(load_library().fa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(L), _ptr(D),
+                                 _ptr(dq_accum), _ptr(dk), _ptr(dv), _stream(stream)), "fa_bwd")
+
+
+def fa_convert_dq(p: FaProblem, dq_accum, dq, stream=None) -> None:
+    _same_layout(p, dq)
+    _accum(p, dq_accum)
+    _check(load_library().fa_convert_dq(ctypes.byref(p), _ptr(dq_accum), _ptr(dq), _stream(stream)),
+           "fa_convert_dq")
+
+
+def fa_backward(p: FaProblem, q, k, v, o, do, L, D, dq_accum, dq, dk, dv, stream=None) -> None:
+    _same_layout(p, q, k, v, o, do, dq, dk, dv)
+    _rows(p, L, D)
+    _accum(p, dq_accum)
+    _check(load_library().fa_backward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(L),
+                                      _ptr(D), _ptr(dq_accum), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),
+           "fa_backward")
+
+
+def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
+    """O, L for contiguous [B, H, N, d] CUDA tensors (bf16 or fp32)."""
+    p = problem_for(q, scale, causal)
+    o = torch.empty_like(q)
+    L = torch.empty((p.B, p.H, p.N), dtype=torch.float32, device=q.device)
+    fa_fwd(p, q, k, v, o, L, stream)
+    return o, L
+
+
+def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, stream=None, workspace=None):
+    """dQ, dK, dV.  ``workspace`` may pass preallocated (D, dq_accum)."""
+    p = problem_for(q, scale, causal)
+    if workspace is None:
+        D = torch.empty((p.B, p.H, p.N), dtype=torch.float32, device=q.device)
+        acc = torch.empty(fa_dq_accum_elems(p), dtype=torch.float32, device=q.device)
+    else:
+        D, acc = workspace
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_backward(p, q, k, v, o, do, L, D, acc, dq, dk, dv, stream)
+    return dq, dk, dv
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word."""
+    code = ctypes.c_int32(0)
+    _check(load_library().fa_get_device_status(_stream(stream), ctypes.byref(code)), "fa_get_device_status")
+    return int(code.value)
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    load_library().fa_set_wait_limit_ns(int(ns))
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load_library().fa_selftest_wait_timeout(int(limit_ns), _stream(stream)), "fa_selftest_wait_timeout")

@@ -1,0 +1,382 @@
+// Host side of libfa: argument validation, the per-device status word, and
+// the two bandwidth-bound kernels of the backward pass (preprocess and
+// convert).  Entry points are declared in include/fa.h.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// ----------------------------------------------------------------------------
+// Device status word: one int per device, in a file-scope __device__ variable.
+// Host code must not hand the symbol itself to a kernel (on the host it only
+// names a shadow); its device address is looked up once per device.
+// ----------------------------------------------------------------------------
+__device__ int32_t g_status_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int32_t* g_status_ptr[kMaxDevices] = {nullptr};
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+}  // namespace
+
+int32_t* device_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+
+// ----------------------------------------------------------------------------
+// Preprocess: D = rowsum(O * dO) in fp32 and zero the dQ accumulator.
+// One block of 256 threads per (b, h, 128-row tile).  Each thread reads 16
+// bytes of O and of dO per step; the lanes that share a row reduce with warp
+// shuffles.  The same block then zeroes that tile of the accumulator
+// (128 * d floats, float4 stores).  Pure HBM streaming.
+// ----------------------------------------------------------------------------
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<float> {
+  static constexpr int kElems = 4;
+  __device__ static float dot(const uint4& a, const uint4& b) {
+    return __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
+           __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
+  }
+};
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  __device__ static float dot2(uint32_t a, uint32_t b) {
+    float a0 = __uint_as_float(a << 16), a1 = __uint_as_float(a & 0xffff0000u);
+    float b0 = __uint_as_float(b << 16), b1 = __uint_as_float(b & 0xffff0000u);
+    return a0 * b0 + a1 * b1;
+  }
+  __device__ static float dot(const uint4& a, const uint4& b) {
+    return dot2(a.x, b.x) + dot2(a.y, b.y) + dot2(a.z, b.z) + dot2(a.w, b.w);
+  }
+};
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ O, const T* __restrict__ dO,
+                                                         float* __restrict__ D, float* __restrict__ dq_accum,
+                                                         int H, int N, int64_t sb, int64_t sh, int64_t sn,
+                                                         int tiles_per_head) {
+  constexpr int kVec = Vec16<T>::kElems;
+  constexpr int kLanesPerRow = HD / kVec;          // 4 .. 32, a power of two
+  constexpr int kRowsPerStep = 256 / kLanesPerRow;
+  constexpr int kSteps = kTileRows / kRowsPerStep;
+  const int tile = blockIdx.x % tiles_per_head;
+  const int bh = blockIdx.x / tiles_per_head;
+  const int b = bh / H, h = bh % H;
+  const int sub = threadIdx.x % kLanesPerRow;
+  const int row_in_step = threadIdx.x / kLanesPerRow;
+  const int64_t head_off = (int64_t)b * sb + (int64_t)h * sh;
+
+  float acc[kSteps];
+#pragma unroll
+  for (int s = 0; s < kSteps; ++s) {
+    const int n = tile * kTileRows + s * kRowsPerStep + row_in_step;
+    acc[s] = 0.f;
+    if (n < N) {
+      const int64_t off = head_off + (int64_t)n * sn + sub * kVec;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(O + off));
+      const uint4 g = __ldg(reinterpret_cast<const uint4*>(dO + off));
+      acc[s] = Vec16<T>::dot(a, g);
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < kSteps; ++s) {
+#pragma unroll
+    for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc[s] += __shfl_xor_sync(0xffffffffu, acc[s], m);
+    const int n = tile * kTileRows + s * kRowsPerStep + row_in_step;
+    if (sub == 0 && n < N) D[(int64_t)bh * N + n] = acc[s];
+  }
+  // zero this tile of the accumulator: 128 * HD floats
+  float4* z = reinterpret_cast<float4*>(dq_accum + ((int64_t)bh * tiles_per_head + tile) * (int64_t)kTileRows * HD);
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int k = threadIdx.x; k < kTileRows * HD / 4; k += 256) z[k] = zero;
+}
+
+template <typename T>
+static cudaError_t launch_preprocess_t(const fa_problem& p, const T* O, const T* dO, float* D, float* acc,
+                                       cudaStream_t s) {
+  const int tiles = (int)ceil_div(p.N, kTileRows);
+  const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
+#define FA_PRE_CASE(HDV)                                                                                    \
+  case HDV:                                                                                                 \
+    preprocess_kernel<T, HDV><<<grid, 256, 0, s>>>(O, dO, D, acc, p.H, p.N, p.stride_b, p.stride_h,        \
+                                                   p.stride_n, tiles);                                      \
+    break;
+  switch (p.d) {
+    FA_PRE_CASE(16)
+    FA_PRE_CASE(32)
+    FA_PRE_CASE(64)
+    FA_PRE_CASE(128)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef FA_PRE_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO, float* D, float* dq_accum,
+                              cudaStream_t s) {
+  if (p.dtype == FA_BF16)
+    return launch_preprocess_t<__nv_bfloat16>(p, (const __nv_bfloat16*)O, (const __nv_bfloat16*)dO, D,
+                                              dq_accum, s);
+  return launch_preprocess_t<float>(p, (const float*)O, (const float*)dO, D, dq_accum, s);
+}
+
+// ----------------------------------------------------------------------------
+// Convert: dQ = T(scale * dq_accum), undoing the tile-blocked layout.  One
+// block per (b, h, 128-row tile): a coalesced read of the tile into shared
+// memory (row-major, padded), then row-contiguous 16-byte output stores.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void store_out(float* dst, const float* v, int n) {
+  for (int i = 0; i < n; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+__device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float* v, int n) {
+  for (int i = 0; i < n; i += 8) {
+    uint4 u;
+    u.x = ptx::pack_bf16x2(v[i], v[i + 1]);
+    u.y = ptx::pack_bf16x2(v[i + 2], v[i + 3]);
+    u.z = ptx::pack_bf16x2(v[i + 4], v[i + 5]);
+    u.w = ptx::pack_bf16x2(v[i + 6], v[i + 7]);
+    *reinterpret_cast<uint4*>(dst + i) = u;
+  }
+}
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict__ acc, T* __restrict__ dQ, int H,
+                                                         int N, int64_t sb, int64_t sh, int64_t sn,
+                                                         int tiles_per_head, float scale) {
+  constexpr int kPitch = HD + 4;  // floats; keeps 16-byte alignment, staggers banks
+  extern __shared__ float4 smem_f4[];
+  float* tile_s = reinterpret_cast<float*>(smem_f4);
+  const int tile = blockIdx.x % tiles_per_head;
+  const int bh = blockIdx.x / tiles_per_head;
+  const int b = bh / H, h = bh % H;
+  const float4* src = reinterpret_cast<const float4*>(acc + ((int64_t)bh * tiles_per_head + tile) * (int64_t)kTileRows * HD);
+  // layout inside a tile: [c/4][row][4]
+#pragma unroll 4
+  for (int k = threadIdx.x; k < kTileRows * HD / 4; k += 256) {
+    const int g = k / kTileRows, r = k % kTileRows;
+    const float4 v = __ldg(src + k);
+    *reinterpret_cast<float4*>(tile_s + r * kPitch + g * 4) = v;
+  }
+  __syncthreads();
+  constexpr int kVec = 16 / sizeof(T);           // outputs per 16-byte store
+  constexpr int kPerRow = HD / kVec;
+  for (int k = threadIdx.x; k < kTileRows * kPerRow; k += 256) {
+    const int r = k / kPerRow, c = (k % kPerRow) * kVec;
+    const int n = tile * kTileRows + r;
+    if (n >= N) continue;
+    float v[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) v[e] = scale * tile_s[r * kPitch + c + e];
+    store_out(dQ + (int64_t)b * sb + (int64_t)h * sh + (int64_t)n * sn + c, v, kVec);
+  }
+}
+
+template <typename T>
+static cudaError_t launch_convert_t(const fa_problem& p, const float* acc, T* dQ, cudaStream_t s) {
+  const int tiles = (int)ceil_div(p.N, kTileRows);
+  const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
+#define FA_CONV_CASE(HDV)                                                                                  \
+  case HDV: {                                                                                              \
+    const size_t sm = (size_t)kTileRows * (HDV + 4) * sizeof(float);                                      \
+    if (sm > 48 * 1024) {                                                                                  \
+      cudaError_t e = cudaFuncSetAttribute(convert_dq_kernel<T, HDV>,                                      \
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);          \
+      if (e != cudaSuccess) return e;                                                                      \
+    }                                                                                                      \
+    convert_dq_kernel<T, HDV><<<grid, 256, sm, s>>>(acc, dQ, p.H, p.N, p.stride_b, p.stride_h, p.stride_n, \
+                                                    tiles, p.scale);                                       \
+    break;                                                                                                 \
+  }
+  switch (p.d) {
+    FA_CONV_CASE(16)
+    FA_CONV_CASE(32)
+    FA_CONV_CASE(64)
+    FA_CONV_CASE(128)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef FA_CONV_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_dq(const fa_problem& p, const float* acc, void* dQ, cudaStream_t s) {
+  if (p.dtype == FA_BF16) return launch_convert_t<__nv_bfloat16>(p, acc, (__nv_bfloat16*)dQ, s);
+  return launch_convert_t<float>(p, acc, (float*)dQ, s);
+}
+
+// ----------------------------------------------------------------------------
+// Failure-detection self test: one warp waits on an mbarrier that nothing
+// arrives at, with the bounded wait used by the tensor-core kernels.
+// ----------------------------------------------------------------------------
+__global__ void selftest_wait_kernel(int32_t* status, uint64_t wait_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_addr(&bar), 1);
+    ptx::fence_mbar_init();
+    abort_flag = 0;
+  }
+  __syncthreads();
+  ptx::Waiter w{&abort_flag, status, wait_ns};
+  // phase 0 never completes: nobody arrives
+  (void)ptx::wait_bounded(ptx::smem_addr(&bar), 0, w, true);
+  __syncthreads();
+}
+
+cudaError_t launch_selftest_wait(int32_t* status, uint64_t wait_ns, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(status, wait_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa
+
+// ============================================================================
+// Public C ABI
+// ============================================================================
+namespace {
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status validate(const fa_problem* p) {
+  if (!p) return FA_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) return FA_ERR_INVALID_ARG;
+  if (p->reserved != 0) return FA_ERR_INVALID_ARG;
+  if (p->causal != 0 && p->causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(p->scale == p->scale) || p->scale <= 0.f || p->scale > 1e30f) return FA_ERR_INVALID_ARG;
+  if (p->dtype != FA_BF16 && p->dtype != FA_FP32) return FA_ERR_INVALID_ARG;
+  if (p->N > (1 << 24) || (int64_t)p->B * p->H > (1 << 24)) return FA_ERR_UNSUPPORTED;
+  const int64_t es = p->dtype == FA_BF16 ? 2 : 4;
+  if (p->stride_n < p->d || p->stride_h < 1 || p->stride_b < 1) return FA_ERR_INVALID_ARG;
+  if ((p->stride_n * es) % 16 || (p->stride_h * es) % 16 || (p->stride_b * es) % 16) return FA_ERR_INVALID_ARG;
+  if (p->dtype == FA_BF16) {
+    if (p->d != 64 && p->d != 128) return FA_ERR_UNSUPPORTED;
+  } else {
+    if (p->d != 16 && p->d != 32 && p->d != 64 && p->d != 128) return FA_ERR_UNSUPPORTED;
+  }
+  return FA_OK;
+}
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_dq_accum_elems(const fa_problem* p) {
+  if (validate(p) != FA_OK) return 0;
+  return (size_t)p->B * p->H * fa::ceil_div(p->N, fa::kTileRows) * fa::kTileRows * p->d;
+}
+
+fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* V, void* O, float* L,
+                 void* stream) {
+  fa_status st = validate(p);
+  if (st != FA_OK) return st;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(L)) return FA_ERR_INVALID_ARG;
+  return from_cuda(fa::launch_fwd_simt(*p, Q, K, V, O, L, (cudaStream_t)stream));
+}
+
+fa_status fa_bwd_preprocess(const fa_problem* p, const void* O, const void* dO, float* D, float* dQ_accum,
+                            void* stream) {
+  fa_status st = validate(p);
+  if (st != FA_OK) return st;
+  if (!aligned16(O) || !aligned16(dO) || !aligned16(D) || !aligned16(dQ_accum)) return FA_ERR_INVALID_ARG;
+  return from_cuda(fa::launch_preprocess(*p, O, dO, D, dQ_accum, (cudaStream_t)stream));
+}
+
+fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* V, const void* dO, const float* L,
+                 const float* D, float* dQ_accum, void* dK, void* dV, void* stream) {
+  fa_status st = validate(p);
+  if (st != FA_OK) return st;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(L) || !aligned16(D) ||
+      !aligned16(dQ_accum) || !aligned16(dK) || !aligned16(dV))
+    return FA_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (p->dtype == FA_FP32)
+    return from_cuda(fa::launch_bwd_simt_fp32(*p, (const float*)Q, (const float*)K, (const float*)V,
+                                              (const float*)dO, L, D, dQ_accum, (float*)dK, (float*)dV, s));
+  int32_t* status = fa::device_status_word();
+  if (!status) return FA_ERR_CUDA;
+  return from_cuda(fa::launch_bwd_sm103(*p, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s));
+}
+
+fa_status fa_convert_dq(const fa_problem* p, const float* dQ_accum, void* dQ, void* stream) {
+  fa_status st = validate(p);
+  if (st != FA_OK) return st;
+  if (!aligned16(dQ_accum) || !aligned16(dQ)) return FA_ERR_INVALID_ARG;
+  return from_cuda(fa::launch_convert_dq(*p, dQ_accum, dQ, (cudaStream_t)stream));
+}
+
+fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const void* V, const void* O,
+                      const void* dO, const float* L, float* D, float* dQ_accum, void* dQ, void* dK, void* dV,
+                      void* stream) {
+  fa_status st = validate(p);
+  if (st != FA_OK) return st;
+  if (!aligned16(dQ)) return FA_ERR_INVALID_ARG;
+  st = fa_bwd_preprocess(p, O, dO, D, dQ_accum, stream);
+  if (st != FA_OK) return st;
+  st = fa_bwd(p, Q, K, V, dO, L, D, dQ_accum, dK, dV, stream);
+  if (st != FA_OK) return st;
+  return fa_convert_dq(p, dQ_accum, dQ, stream);
+}
+
+fa_status fa_get_device_status(void* stream, int32_t* code) {
+  if (!code) return FA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FA_ERR_CUDA;
+  int32_t* word = fa::device_status_word();
+  if (!word) return FA_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  const int32_t zero = 0;
+  if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  *code = v;
+  return FA_OK;
+}
+
+void fa_set_wait_limit_ns(uint64_t ns) { fa::g_wait_ns.store(ns == 0 ? 1 : ns); }
+
+fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  int32_t* status = fa::device_status_word();
+  if (!status) return FA_ERR_CUDA;
+  return from_cuda(fa::launch_selftest_wait(status, limit_ns, (cudaStream_t)stream));
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported problem";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+    case FA_ERR_DEVICE: return "device self check failed";
+  }
+  return "unknown status";
+}
+
+int32_t fa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,506 @@
+// FlashAttention-2 backward for bf16, head dim 64 or 128, on the sm_100-family
+// tensor cores (tcgen05 MMA with accumulators in tensor memory, operands
+// staged in shared memory by TMA).
+//
+// Loop order follows "CUDA 算子工程" ch.16 §16.2: one CTA owns a 128-row key
+// block K_j, V_j (resident in shared memory) and walks the 128-row query
+// blocks Q_i, dO_i.  dV_j and dK_j accumulate in tensor memory and are
+// written once; dQ partials leave through fire-and-forget fp32 vector
+// reductions into the tile-blocked accumulator (§16.3, scheme A').  Under the
+// causal mask the walk starts at the diagonal block, so fully masked pairs
+// are never loaded (§16.8 item 2).
+//
+// The scores are computed transposed, S^T = K_j Q_i^T, so that TMEM lane r is
+// key row r: P^T and dS^T then sit with keys as the M dimension, which is
+// what dV += P^T dO and dK += dS^T Q need, and P^T can feed the dV product
+// straight from tensor memory.
+//
+// Warp roles (320 threads):
+//   warps 0-3  "softmax": one thread per key row.  P = exp2(S*scale*log2e -
+//              L*log2e) -> bf16 into TMEM; dS = P * (dP - D) -> bf16 into
+//              shared memory (128-byte swizzle).  Epilogue: dV.
+//   warps 4-7  "dQ": drain the dQ tile from TMEM, reduce into global memory.
+//              Epilogue: dK * scale.
+//   warp  8    TMA producer (K, V once; Q, dO double-buffered) and the L, D
+//              rows of each query block.
+//   warp  9    TMEM allocator; lane 0 issues every MMA.
+//
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [0,128)    S^T, then P^T (bf16, columns [0,64)) written over it
+//   [128,256)  dP^T, then the dQ tile of the same step written over it
+//   [256,256+d) dV accumulator, [256+d,256+2d) dK accumulator
+//
+// MMA issue order per query block i (software pipelined):
+//   dV(i)  dP(i)  S(i+1)  dK(i)  dQ(i)
+// so the tensor pipe works on S(i+1) while the softmax warps turn dP(i) into
+// dS(i), and on dK(i), dQ(i), dV(i+1) while they turn S(i+1) into P(i+1).
+//
+// Every wait is bounded; when one runs out the CTA records FA_ERR_TIMEOUT,
+// drains its own TMA loads and MMAs, frees tensor memory and exits.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBlk = 128;  // Br = Bc = 128
+constexpr int kThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum BarId {
+  KV_FULL = 0,  // K, V landed
+  FULL0,        // query stage 0 (Q, dO, L, D) landed
+  FULL1,
+  EMPTY0,       // query stage 0 free again
+  EMPTY1,
+  S_FULL,       // S^T(i) in TMEM
+  P_FULL,       // P^T(i) in TMEM (128 arrivals)
+  DV_DONE,      // dV(i) product done: S/P columns reusable
+  DP_FULL,      // dP^T(i) in TMEM
+  DS_FULL,      // dS^T(i) in shared memory (128 arrivals)
+  DQ_FULL,      // dQ(i) in TMEM and dS(i) consumed
+  DQ_EMPTY,     // dQ(i) drained from TMEM (128 arrivals)
+  ACC_FULL,     // every MMA done: dK, dV final
+  kNumBars
+};
+
+template <int HD>
+struct Layout {
+  static constexpr int kChunk = kBlk * 128;     // 128 rows x 128 bytes (64 bf16 columns)
+  static constexpr int kTile = kBlk * HD * 2;   // one Q / K / V / dO tile
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTile;
+  static constexpr int kQ = kV + kTile;         // 2 stages
+  static constexpr int kdO = kQ + 2 * kTile;    // 2 stages
+  static constexpr int kdS = kdO + 2 * kTile;   // 128 x 128 bf16, two 64-column chunks
+  static constexpr int kL = kdS + 2 * kChunk;   // 2 stages x 128 fp32 (L * log2 e)
+  static constexpr int kD = kL + 2 * kBlk * 4;  // 2 stages x 128 fp32
+  static constexpr int kBar = kD + 2 * kBlk * 4;
+  static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM base address, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr uint32_t kColS = 0, kColP = 0, kColdP = 128, kColdQ = 128;
+  static constexpr uint32_t kColdV = 256, kColdK = 256 + HD;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kBytes <= 232448, "shared memory budget");
+};
+
+struct BwdParams {
+  const float* L;
+  const float* D;
+  float* dq_accum;
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  int32_t* status;
+  uint64_t wait_ns;
+  int B, H, N;
+  int n_tiles;  // ceil(N / 128), for both queries and keys
+  int64_t sb, sh, sn;
+  float scale;
+  int causal;
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const ptx::Waiter& w) {
+  // all lanes leave together so that .sync.aligned tcgen05 ops stay converged
+  return __all_sync(0xffffffffu, ptx::wait_bounded(bar, parity, w, true));
+}
+
+// TMEM row (this thread's lane) of HD fp32 values -> bf16 row in global.
+template <int HD>
+__device__ __forceinline__ void store_row(uint32_t taddr, bool valid, __nv_bfloat16* dst, float mul) {
+#pragma unroll
+  for (int c = 0; c < HD / 32; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld32(taddr + c * 32, r);
+    if (valid) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint4 v;
+        v.x = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 0]) * mul, __uint_as_float(r[8 * u + 1]) * mul);
+        v.y = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul);
+        v.z = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul);
+        v.w = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul);
+        *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = v;
+      }
+    }
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const BwdParams prm) {
+  using Ly = Layout<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicCAS(prm.status, 0, (int32_t)FA_ERR_DEVICE);
+    return;
+  }
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kMisc + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + Ly::kBar + 8 * i; };
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(KV_FULL), 1);
+    ptx::mbar_init(bar(FULL0), 32);
+    ptx::mbar_init(bar(FULL1), 32);
+    ptx::mbar_init(bar(EMPTY0), 1);
+    ptx::mbar_init(bar(EMPTY1), 1);
+    ptx::mbar_init(bar(S_FULL), 1);
+    ptx::mbar_init(bar(P_FULL), 128);
+    ptx::mbar_init(bar(DV_DONE), 1);
+    ptx::mbar_init(bar(DP_FULL), 1);
+    ptx::mbar_init(bar(DS_FULL), 128);
+    ptx::mbar_init(bar(DQ_FULL), 1);
+    ptx::mbar_init(bar(DQ_EMPTY), 128);
+    ptx::mbar_init(bar(ACC_FULL), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(sbase + Ly::kMisc, Ly::kTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // work item: key block kb of head (b, h); key block 0 first (longest walk)
+  const int BH = prm.B * prm.H;
+  const int kb = blockIdx.x / BH;
+  const int bh = blockIdx.x % BH;
+  const int b = bh / prm.H, h = bh % prm.H;
+  const int k0 = kb * kBlk;
+  const int q_first = prm.causal ? kb : 0;
+  const int n_iter = prm.n_tiles - q_first;
+  const int64_t head = (int64_t)b * prm.sb + (int64_t)h * prm.sh;
+  const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
+
+  const uint32_t sK = sbase + Ly::kK, sV = sbase + Ly::kV, sdS = sbase + Ly::kdS;
+  auto sQ = [&](int st) -> uint32_t { return sbase + Ly::kQ + st * Ly::kTile; };
+  auto sdO = [&](int st) -> uint32_t { return sbase + Ly::kdO + st * Ly::kTile; };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    int issued = 0;
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmQ);
+      ptx::prefetch_tensormap(&tmK);
+      ptx::prefetch_tensormap(&tmV);
+      ptx::prefetch_tensormap(&tmdO);
+      ptx::mbar_arrive_expect_tx(bar(KV_FULL), 2 * Ly::kTile);
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {
+        ptx::tma_load_4d(sK + c * Ly::kChunk, &tmK, bar(KV_FULL), c * 64, k0, h, b);
+        ptx::tma_load_4d(sV + c * Ly::kChunk, &tmV, bar(KV_FULL), c * 64, k0, h, b);
+      }
+    }
+    for (int i = 0; i < n_iter; ++i) {
+      const int st = i & 1;
+      if (i >= 2) {
+        ok = warp_wait(bar(EMPTY0 + st), ((i - 2) >> 1) & 1, W);
+        if (!ok) break;
+      }
+      const int q0 = (q_first + i) * kBlk;
+      float* sL = reinterpret_cast<float*>(smem + Ly::kL) + st * kBlk;
+      float* sD = reinterpret_cast<float*>(smem + Ly::kD) + st * kBlk;
+      for (int r = lane; r < kBlk; r += 32) {
+        const int q = q0 + r;
+        sL[r] = q < prm.N ? prm.L[(int64_t)bh * prm.N + q] * kLog2e : INFINITY;
+        sD[r] = q < prm.N ? prm.D[(int64_t)bh * prm.N + q] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(FULL0 + st), 2 * Ly::kTile);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c) {
+          ptx::tma_load_4d(sQ(st) + c * Ly::kChunk, &tmQ, bar(FULL0 + st), c * 64, q0, h, b);
+          ptx::tma_load_4d(sdO(st) + c * Ly::kChunk, &tmdO, bar(FULL0 + st), c * 64, q0, h, b);
+        }
+      } else {
+        ptx::mbar_arrive(bar(FULL0 + st));
+      }
+      issued = i + 1;
+    }
+    if (!ok) {  // let every copy this CTA started land before the CTA exits
+      ptx::wait_bounded(bar(KV_FULL), 0, W, false);
+      for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+        ptx::wait_bounded(bar(FULL0 + (i & 1)), (i >> 1) & 1, W, false);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdKV = ptx::idesc_bf16_f32(128, HD, false, true);   // dV, dK
+      constexpr uint32_t kIdQ = ptx::idesc_bf16_f32(128, HD, true, true);     // dQ
+      // K-major operand: 16-element K step kk inside 64-column chunks
+      auto kdesc = [&](uint32_t tile, int kk) -> uint64_t {
+        return ptx::sdesc_sw128(tile + (kk >> 2) * Ly::kChunk + (kk & 3) * 32, 16, 1024);
+      };
+      // MN-major operand: 16-row K step kk; 64-column MN blocks one chunk apart
+      auto mndesc = [&](uint32_t tile, int kk) -> uint64_t {
+        return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
+      };
+      const uint32_t tS = tmem + Ly::kColS, tP = tmem + Ly::kColP, tdP = tmem + Ly::kColdP;
+      const uint32_t tdQ = tmem + Ly::kColdQ, tdV = tmem + Ly::kColdV, tdK = tmem + Ly::kColdK;
+
+      bool ok = ptx::wait_bounded(bar(KV_FULL), 0, W, true) && ptx::wait_bounded(bar(FULL0), 0, W, true);
+      if (ok) {
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS, kdesc(sK, kk), kdesc(sQ(0), kk), kIdS, kk > 0);
+        ptx::tc_commit(bar(S_FULL));
+      }
+      for (int i = 0; ok && i < n_iter; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = i & 1;
+        // dV += P^T dO   (A = P^T from TMEM)
+        if (!(ok = ptx::wait_bounded(bar(P_FULL), ph, W, true))) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          ptx::mma_ts(tdV, tP + kk * 8, mndesc(sdO(st), kk), kIdKV, (i | kk) != 0);
+        ptx::tc_commit(bar(DV_DONE));
+        // dP^T = V dO^T  (its columns held dQ(i-1): wait until drained)
+        if (i > 0) {
+          if (!(ok = ptx::wait_bounded(bar(DQ_EMPTY), (i - 1) & 1, W, true))) break;
+          ptx::tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tdP, kdesc(sV, kk), kdesc(sdO(st), kk), kIdS, kk > 0);
+        ptx::tc_commit(bar(DP_FULL));
+        // S^T(i+1) = K Q(i+1)^T once dV(i) has read P(i)
+        if (i + 1 < n_iter) {
+          if (!(ok = ptx::wait_bounded(bar(FULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W, true))) break;
+          if (!(ok = ptx::wait_bounded(bar(DV_DONE), ph, W, true))) break;
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            ptx::mma_ss(tS, kdesc(sK, kk), kdesc(sQ(st ^ 1), kk), kIdS, kk > 0);
+          ptx::tc_commit(bar(S_FULL));
+        }
+        // dK += dS^T Q ;  dQ = dS K
+        if (!(ok = ptx::wait_bounded(bar(DS_FULL), ph, W, true))) break;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          ptx::mma_ss(tdK, kdesc(sdS, kk), mndesc(sQ(st), kk), kIdKV, (i | kk) != 0);
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk) ptx::mma_ss(tdQ, mndesc(sdS, kk), mndesc(sK, kk), kIdQ, kk > 0);
+        ptx::tc_commit(bar(DQ_FULL));
+        ptx::tc_commit(bar(EMPTY0 + st));
+      }
+      ptx::tc_commit(bar(ACC_FULL));
+      if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax / dS
+    const int t = threadIdx.x;  // key row within the block == TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int kr = k0 + t;
+    const bool key_ok = kr < prm.N;
+    const float sl2 = prm.scale * kLog2e;
+    bool ok = true;
+    for (int i = 0; i < n_iter; ++i) {
+      const int st = i & 1;
+      const uint32_t ph = i & 1;
+      const int q0 = (q_first + i) * kBlk;
+      if (!(ok = warp_wait(bar(S_FULL), ph, W))) break;
+      if (!(ok = warp_wait(bar(FULL0 + st), (i >> 1) & 1, W))) break;
+      ptx::tc_fence_after();
+      const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4;
+      const bool diag = prm.causal && q0 == k0;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tmem + Ly::kColS + lane_off + c * 32, r);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const int col = c * 32 + j;
+          const float4 l4 = ptx::ld_shared_f4(sLa + col * 4);
+          float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
+          float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
+          float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
+          float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
+          if (diag) {  // key k0 + t is visible to query q0 + col iff t <= col
+            p0 = col + 0 < t ? 0.f : p0;
+            p1 = col + 1 < t ? 0.f : p1;
+            p2 = col + 2 < t ? 0.f : p2;
+            p3 = col + 3 < t ? 0.f : p3;
+          }
+          pk[c * 16 + j / 2] = ptx::pack_bf16x2(p0, p1);
+          pk[c * 16 + j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+        }
+      }
+      if (!key_ok) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) pk[k] = 0u;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_st16(tmem + Ly::kColP + lane_off + c * 16, &pk[c * 16]);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(P_FULL));
+
+      if (!(ok = warp_wait(bar(DP_FULL), ph, W))) break;
+      if (i > 0 && !(ok = warp_wait(bar(DQ_FULL), (i - 1) & 1, W))) break;  // dS(i-1) consumed
+      ptx::tc_fence_after();
+      const uint32_t sDa = sbase + Ly::kD + st * kBlk * 4;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tmem + Ly::kColdP + lane_off + c * 32, r);
+        uint32_t ds[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 d4 = ptx::ld_shared_f4(sDa + (c * 32 + j) * 4);
+          const uint32_t pa = pk[c * 16 + j / 2], pb = pk[c * 16 + j / 2 + 1];
+          const float ds0 = ptx::bf16lo(pa) * (__uint_as_float(r[j + 0]) - d4.x);
+          const float ds1 = ptx::bf16hi(pa) * (__uint_as_float(r[j + 1]) - d4.y);
+          const float ds2 = ptx::bf16lo(pb) * (__uint_as_float(r[j + 2]) - d4.z);
+          const float ds3 = ptx::bf16hi(pb) * (__uint_as_float(r[j + 3]) - d4.w);
+          ds[j / 2] = ptx::pack_bf16x2(ds0, ds1);
+          ds[j / 2 + 1] = ptx::pack_bf16x2(ds2, ds3);
+        }
+        // row t of dS^T, query columns [32c, 32c + 32): 4 x 16-byte pieces,
+        // 128-byte swizzle (piece index XOR row % 8)
+        const uint32_t row = sdS + (c >> 1) * Ly::kChunk + t * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t piece = (uint32_t)((c & 1) * 4 + u);
+          ptx::st_shared_v4(row + ((piece ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1], ds[4 * u + 2],
+                            ds[4 * u + 3]);
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(DS_FULL));
+    }
+    if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
+      ptx::tc_fence_after();
+      store_row<HD>(tmem + Ly::kColdV + lane_off, key_ok, prm.dV + head + (int64_t)kr * prm.sn, 1.0f);
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain
+    const int t = threadIdx.x - 128;  // query row within the block == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    bool ok = true;
+    for (int i = 0; i < n_iter; ++i) {
+      if (!(ok = warp_wait(bar(DQ_FULL), i & 1, W))) break;
+      ptx::tc_fence_after();
+      uint32_t r[HD];
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c)
+        ptx::tmem_ld32(tmem + Ly::kColdQ + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(DQ_EMPTY));
+      const int qt = q_first + i;
+      float* base = prm.dq_accum + ((int64_t)bh * prm.n_tiles + qt) * (int64_t)(kBlk * HD) + t * 4;
+#pragma unroll
+      for (int g = 0; g < HD / 4; ++g)
+        ptx::red_add_v4(base + g * (kBlk * 4), __uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                        __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+    }
+    const int kr = k0 + t;
+    if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
+      ptx::tc_fence_after();
+      store_row<HD>(tmem + Ly::kColdK + lane_off, kr < prm.N, prm.dK + head + (int64_t)kr * prm.sn, prm.scale);
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, Ly::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [B, H, N, d] bf16 tensor as a 4-D TMA map with 64 x 128 boxes, 128-byte
+// swizzle; rows past N read as zeros.
+bool make_map(CUtensorMap* m, const void* base, const fa_problem& p) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)p.H, (cuuint64_t)p.B};
+  cuuint64_t strides[3] = {(cuuint64_t)p.stride_n * 2, (cuuint64_t)p.stride_h * 2, (cuuint64_t)p.stride_b * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)kBlk, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int HD>
+cudaError_t launch_hd(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t s) {
+  using Ly = Layout<HD>;
+  cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
+  bwd_sm103_kernel<HD><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
+                             const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
+                             uint64_t wait_ns, cudaStream_t s) {
+  CUtensorMap maps[4];
+  if (!make_map(&maps[0], Q, p) || !make_map(&maps[1], K, p) || !make_map(&maps[2], V, p) ||
+      !make_map(&maps[3], dO, p))
+    return cudaErrorInvalidValue;
+  BwdParams prm;
+  prm.L = L;
+  prm.D = D;
+  prm.dq_accum = dq_accum;
+  prm.dK = (__nv_bfloat16*)dK;
+  prm.dV = (__nv_bfloat16*)dV;
+  prm.status = status;
+  prm.wait_ns = wait_ns;
+  prm.B = p.B;
+  prm.H = p.H;
+  prm.N = p.N;
+  prm.n_tiles = (int)ceil_div(p.N, kBlk);
+  prm.sb = p.stride_b;
+  prm.sh = p.stride_h;
+  prm.sn = p.stride_n;
+  prm.scale = p.scale;
+  prm.causal = p.causal;
+  if (p.d == 64) return launch_hd<64>(p, maps, prm, s);
+  if (p.d == 128) return launch_hd<128>(p, maps, prm, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,45 @@
+// Internal declarations shared by the translation units of libfa.
+// Nothing here is part of the public ABI (include/fa.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Query/key tile height used by the dQ accumulator layout and by the
+// tensor-core kernels.
+constexpr int kTileRows = 128;
+
+// Device status word codes are the fa_status values.
+struct DeviceStatus {
+  int32_t* word;  // device address of this device's status word
+};
+
+// Resolved once per device by the API layer.
+int32_t* device_status_word();
+
+// Wait limit (ns) used by every bounded wait in device code.
+uint64_t wait_limit_ns();
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---- launchers (return a cudaError_t from the launch) -------------------
+cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO, float* D,
+                              float* dq_accum, cudaStream_t s);
+cudaError_t launch_convert_dq(const fa_problem& p, const float* dq_accum, void* dQ, cudaStream_t s);
+cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
+                            void* O, float* L, cudaStream_t s);
+cudaError_t launch_bwd_simt_fp32(const fa_problem& p, const float* Q, const float* K, const float* V,
+                                 const float* dO, const float* L, const float* D, float* dq_accum,
+                                 float* dK, float* dV, cudaStream_t s);
+// tcgen05 / TMEM / TMA backward for bf16, d in {64, 128}.  Returns
+// cudaErrorInvalidValue if a tensor map cannot be encoded.
+cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V,
+                             const void* dO, const float* L, const float* D, float* dq_accum,
+                             void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
+cudaError_t launch_selftest_wait(int32_t* status, uint64_t wait_ns, cudaStream_t s);
+
+}  // namespace fa

@@ -1,0 +1,152 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 backward library.
+ *
+ * The library computes the backward pass of scaled-dot-product attention
+ *
+ *     S = scale * Q K^T,   P = softmax(S) row-wise,   O = P V
+ *
+ * without ever storing an N x N matrix: S and P are recomputed tile by tile
+ * on chip from Q, K and the per-row logsumexp L saved by the forward pass
+ * ("CUDA 算子工程" ch.16 "FA2 反向", §16.2 loop order and §16.4 role of LSE).
+ *
+ * A backward pass is three calls on one stream:
+ *     fa_bwd_preprocess   D = rowsum(O * dO), zero the fp32 dQ accumulator
+ *     fa_bwd              dK, dV written once per key block; dQ partials
+ *                         reduced into the fp32 accumulator
+ *     fa_convert_dq       dQ = scale * accumulator, cast to the output dtype
+ * and fa_fwd produces O and L for it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d] tensors of `dtype` with the
+ *    last dimension contiguous and element strides stride_b, stride_h,
+ *    stride_n (identical for all eight tensors).  N_q == N_k == N.
+ *  - L and D are dense [B, H, N] float32 arrays (row-major, no padding).
+ *  - The dQ accumulator is a float32 array of fa_dq_accum_elems() elements in
+ *    a tile-blocked layout (below).  It belongs to the caller like every
+ *    other buffer: the library never allocates device memory and keeps only
+ *    one 4-byte device status word per device.
+ *  - All pointers are device pointers that the current CUDA device can
+ *    access, 16-byte aligned; every byte stride (stride * element size) must
+ *    be a multiple of 16.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All calls are asynchronous on that stream.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    rejected call launches nothing and returns FA_ERR_INVALID_ARG or
+ *    FA_ERR_UNSUPPORTED.  A failed launch returns FA_ERR_CUDA.  Errors found
+ *    on the device (a bounded wait that ran out, a failed self check) never
+ *    trap: the kernel records a code in the device status word and returns;
+ *    read it with fa_get_device_status().
+ *  - Results are not bitwise reproducible from run to run: dQ partial sums
+ *    reach the accumulator in whatever order the hardware completes its
+ *    reductions (the FA2 default; ch.16 §16.3 notes deterministic=False).
+ *
+ * Supported problems: dtype FA_BF16 with d in {64, 128} (tcgen05 tensor-core
+ * kernels), dtype FA_FP32 with d in {16, 32, 64, 128} (exact fp32 FFMA
+ * kernels, no TF32).  N >= 1, B >= 1, H >= 1, N <= 2^24, B*H <= 2^24.
+ *
+ * dQ accumulator layout
+ * ---------------------
+ * Query rows are grouped into tiles of 128 rows; the last tile of a head is
+ * padded to 128 rows.  Element (b, h, n, c) lives at float index
+ *
+ *   ((((b*H + h) * T + n/128) * (d/4) + c/4) * 128 + n%128) * 4 + c%4
+ *
+ * with T = ceil(N/128), so 32 consecutive rows of one 4-column group are 512
+ * contiguous bytes.  Padding rows receive only zero contributions.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or stride   */
+  FA_ERR_UNSUPPORTED = 2,  /* valid problem outside the supported set        */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed           */
+  FA_ERR_TIMEOUT = 4,      /* device: a bounded wait ran out                 */
+  FA_ERR_DEVICE = 5        /* device: a kernel self check failed             */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
+
+typedef struct {
+  int32_t B, H, N, d;
+  float scale;      /* softmax scale, normally 1/sqrt(d) */
+  int32_t causal;   /* 1: key j visible to query i iff j <= i (top-left) */
+  int32_t dtype;    /* fa_dtype of Q, K, V, O, dO, dQ, dK, dV */
+  int32_t reserved; /* must be 0 */
+  int64_t stride_b, stride_h, stride_n; /* element strides; d is contiguous */
+} fa_problem;
+
+/* Number of float32 elements of the dQ accumulator for problem p
+ * (B * H * ceil(N/128) * 128 * d), or 0 if p is NULL or invalid. */
+size_t fa_dq_accum_elems(const fa_problem* p);
+
+/* Forward pass, companion of the backward: O = softmax(scale Q K^T) V and
+ * L = logsumexp of each row of scale Q K^T (natural log).  Online softmax
+ * over key blocks with running max m, sum l and rescale alpha = exp(m - m')
+ * (1point3acres FlashAttention write-up, online-softmax paragraphs; ch.16
+ * §16.4 L = m + log l).  Reads Q, K, V; writes O (dtype) and L (float32). */
+fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* V,
+                 void* O, float* L, void* stream);
+
+/* Backward preprocess (ch.16 §16.8 item 1; identity of §16.1):
+ * D[b,h,n] = sum_c O[b,h,n,c] * dO[b,h,n,c] in float32, and dQ_accum := 0.
+ * Reads O, dO; writes D and every element of dQ_accum. */
+fa_status fa_bwd_preprocess(const fa_problem* p, const void* O, const void* dO,
+                            float* D, float* dQ_accum, void* stream);
+
+/* Main backward (ch.16 §16.2, §16.3, §16.6): for each key block K_j, V_j,
+ * for each query block Q_i that the causal mask leaves partly visible:
+ *   S = scale Q_i K_j^T, P = exp(S - L_i) (masked entries 0),
+ *   dV_j += P^T dO_i,  dP = dO_i V_j^T,  dS = P * (dP - D_i),
+ *   dQ_accum[i] += dS K_j  (fire-and-forget float32 reductions, no scale),
+ *   dK_j += dS^T Q_i.
+ * Writes dV_j and scale * dK_j once per key block.  dQ_accum must hold the
+ * zeros written by fa_bwd_preprocess (or earlier partial sums to add to). */
+fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* V,
+                 const void* dO, const float* L, const float* D, float* dQ_accum,
+                 void* dK, void* dV, void* stream);
+
+/* dQ = dtype(scale * dQ_accum) (ch.16 §16.3: the convert kernel applies the
+ * softmax scale and casts).  Reads dQ_accum, writes dQ. */
+fa_status fa_convert_dq(const fa_problem* p, const float* dQ_accum, void* dQ, void* stream);
+
+/* The three backward calls in order: preprocess, bwd, convert. */
+fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const void* V,
+                      const void* O, const void* dO, const float* L, float* D,
+                      float* dQ_accum, void* dQ, void* dK, void* dV, void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word.  *code receives FA_OK or the first device-side error recorded since
+ * the last read.  Returns FA_ERR_CUDA if the synchronisation fails. */
+fa_status fa_get_device_status(void* stream, int32_t* code);
+
+/* Upper bound, in nanoseconds, of every wait inside the tensor-core kernels
+ * (default 2e9).  After it runs out a kernel records FA_ERR_TIMEOUT, drains
+ * its own copies in flight, frees its tensor memory and returns. */
+void fa_set_wait_limit_ns(uint64_t ns);
+
+/* Failure-detection self test: launches one block that waits on an
+ * mbarrier no thread ever arrives at, with the same bounded wait the
+ * tensor-core kernels use and a limit of `limit_ns`.  The device status word
+ * then holds FA_ERR_TIMEOUT. */
+fa_status fa_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+const char* fa_status_string(fa_status s);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,119 @@
+"""GPU parity of the tcgen05 bf16 backward against the float64 oracle.
+
+Small problems (ragged tails, causal diagonals, N = 1, d = 64 and 128) are
+compared on every head; the five workloads run at full size in the same
+launch configuration the benchmark times and are compared on sampled heads,
+with shape-free properties (finite values, sum_j dK_j = 0,
+sum_j dV_j = sum_i dO_i) checked on every head.  Tolerance: max|dX - ref| /
+max|ref| <= 2e-2 per tensor, L <= 1e-3."""
+
+import numpy as np
+import pytest
+import torch
+
+import flashattention_backward_gb300 as fa
+from fa_inputs import to_f64, workload
+from gpu_common import compare_head, run_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fa.load_library()
+    assert fa.get_device_status() == 0
+
+
+SMALL = [
+    # B, H, N, d, causal
+    (1, 2, 128, 64, False),
+    (1, 2, 128, 128, True),
+    (1, 1, 1, 64, True),
+    (1, 1, 1, 128, False),
+    (2, 2, 129, 128, True),
+    (1, 3, 300, 64, True),
+    (1, 2, 384, 128, False),
+    (2, 1, 1000, 128, True),
+    (1, 2, 640, 64, False),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL)
+def test_bf16_backward_small(B, H, N, d, causal):
+    w = workload("causal", B=B, H=H, N=N, d=d, causal=causal, seed=100 + N + d)
+    out = run_gpu(w, DEV)
+    assert out["status"] == 0
+    for b in range(B):
+        for h in range(H):
+            compare_head(out, w, b, h, TOL)
+
+
+def test_bf16_backward_large_logits():
+    """Peaky softmax: queries with std 4 as in the long-context workload."""
+    w = workload("long", N=700, H=2, seed=21)
+    out = run_gpu(w, DEV)
+    assert out["status"] == 0
+    for h in range(2):
+        compare_head(out, w, 0, h, TOL)
+
+
+def test_bf16_backward_strided_layout():
+    """[B, N, H, d] storage passed through strides."""
+    B, H, N, d = 2, 3, 200, 64
+    w = workload("causal", B=B, H=H, N=N, d=d, causal=True, seed=31)
+    gen = torch.Generator().manual_seed(31)
+    base = [torch.randn(B, N, H, d, generator=gen).to(torch.bfloat16) for _ in range(4)]
+    q, k, v, g = (t.permute(0, 2, 1, 3).to(DEV) for t in base)  # views with stride_n = H*d
+    assert q.stride(2) == H * d
+    o = torch.empty_like(q)
+    L = torch.empty(B, H, N, device=DEV)
+    p = fa.problem_for(q, w.scale, True)
+    fa.fa_fwd(p, q, k, v, o, L)
+    D = torch.empty(B, H, N, device=DEV)
+    acc = torch.empty(fa.fa_dq_accum_elems(p), device=DEV)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    fa.fa_backward(p, q, k, v, o, g, L, D, acc, dq, dk, dv)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == 0
+    out = dict(q=q.cpu(), k=k.cpu(), v=v.cpu(), g=g.cpu(), o=o.cpu(), L=L.cpu(), dq=dq.cpu(), dk=dk.cpu(),
+               dv=dv.cpu())
+    for b in range(B):
+        for h in range(H):
+            compare_head(out, w, b, h, TOL)
+
+
+def _properties(out, w):
+    dk = to_f64(out["dk"])
+    dv = to_f64(out["dv"])
+    g = to_f64(out["g"])
+    for name in ("o", "L", "dq", "dk", "dv"):
+        assert torch.isfinite(out[name].float()).all(), name
+    # rows of dS sum to 0  ->  sum over keys of dK is 0 (up to rounding)
+    s = np.abs(dk.sum(axis=2)).max(axis=-1)
+    a = np.abs(dk).sum(axis=2).max(axis=-1)
+    assert np.all(s <= 2e-2 * a), float((s / a).max())
+    # rows of P sum to 1  ->  sum over keys of dV equals sum over queries of dO
+    lhs, rhs = dv.sum(axis=2), g.sum(axis=2)
+    assert np.abs(lhs - rhs).max() <= TOL * np.abs(rhs).max()
+
+
+WORKLOADS = [
+    ("mha", [(0, 0), (0, 17), (0, 31)]),
+    ("causal", [(0, 0), (0, 21)]),
+    ("ragged", [(0, 0), (3, 15)]),
+    ("long", [(0, 5)]),
+]
+
+
+@pytest.mark.parametrize("name,heads", WORKLOADS, ids=[w[0] for w in WORKLOADS])
+def test_workload_full_size(name, heads):
+    w = workload(name)
+    out = run_gpu(w, DEV)
+    assert out["status"] == 0
+    _properties(out, w)
+    for b, h in heads:
+        compare_head(out, w, b, h, TOL)

@@ -1,0 +1,123 @@
+"""GPU parity of the bandwidth kernels, the forward and the fp32 backward
+against the float64 oracle, plus the device status / bounded-wait checks."""
+
+import numpy as np
+import pytest
+import torch
+
+import flashattention_backward_gb300 as fa
+from fa_inputs import make_inputs, to_f64, workload
+from gpu_common import compare_head, ratio, run_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fa.load_library()
+    assert fa.get_device_status() == 0
+
+
+def _accum_index(B, H, N, d):
+    """Float index of element (b, h, n, c) in the tile-blocked accumulator
+    layout that include/fa.h documents."""
+    T = -(-N // 128)
+    b, h, n, c = np.meshgrid(np.arange(B), np.arange(H), np.arange(N), np.arange(d), indexing="ij")
+    return ((((b * H + h) * T + n // 128) * (d // 4) + c // 4) * 128 + n % 128) * 4 + c % 4
+
+
+@pytest.mark.parametrize("dtype,d,N", [(torch.bfloat16, 64, 300), (torch.bfloat16, 128, 129),
+                                       (torch.float32, 16, 48), (torch.float32, 128, 1)])
+def test_preprocess_computes_D_and_zeroes_accumulator(dtype, d, N):
+    B, H = 2, 3
+    gen = torch.Generator().manual_seed(5)
+    o = torch.randn(B, H, N, d, generator=gen).to(dtype)
+    do = torch.randn(B, H, N, d, generator=gen).to(dtype)
+    p = fa.problem_for(o, 0.1, False)
+    D = torch.full((B, H, N), float("nan"), device=DEV)
+    acc = torch.full((fa.fa_dq_accum_elems(p),), float("nan"), device=DEV)
+    fa.fa_bwd_preprocess(p, o.to(DEV), do.to(DEV), D, acc)
+    torch.cuda.synchronize()
+    ref = np.sum(to_f64(o) * to_f64(do), axis=-1)
+    np.testing.assert_allclose(to_f64(D), ref, rtol=1e-5, atol=1e-5)
+    assert torch.count_nonzero(acc).item() == 0
+
+
+@pytest.mark.parametrize("dtype,d,N", [(torch.bfloat16, 128, 300), (torch.bfloat16, 64, 128),
+                                       (torch.float32, 16, 48), (torch.float32, 32, 257)])
+def test_convert_undoes_the_documented_layout(dtype, d, N):
+    B, H = 2, 2
+    q = torch.empty(B, H, N, d, dtype=dtype)
+    p = fa.problem_for(q, 0.37, False)
+    gen = torch.Generator().manual_seed(6)
+    acc = torch.randn(fa.fa_dq_accum_elems(p), generator=gen)
+    dq = torch.empty(B, H, N, d, dtype=dtype, device=DEV)
+    fa.fa_convert_dq(p, acc.to(DEV), dq)
+    torch.cuda.synchronize()
+    idx = _accum_index(B, H, N, d)
+    expect = (torch.from_numpy(acc.numpy()[idx]) * torch.tensor(0.37, dtype=torch.float32)).to(dtype)
+    assert torch.equal(dq.cpu(), expect)  # bitwise: same fp32 product, same RNE cast
+
+
+def test_forward_four_numbers_across_a_tile_boundary():
+    """The write-up's four-number example spread over two 64-key tiles:
+    scores 0 then 10, values 0 then 1 -> 0.9999546 (not the 0.5 of a naive
+    per-block average); the second tile brings the new row maximum."""
+    N, d = 128, 16
+    q = torch.zeros(1, 1, N, d)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, 1, N, d)
+    k[0, 0, 64:, 0] = 10.0
+    v = torch.zeros(1, 1, N, d)
+    v[0, 0, 64:, :] = 1.0
+    o, L = fa.attention_forward(q.to(DEV), k.to(DEV), v.to(DEV), 1.0, False)
+    torch.cuda.synchronize()
+    assert abs(o[0, 0, 0, 0].item() - 0.9999546) < 5e-7
+    assert abs(L[0, 0, 0].item() - (10 + np.log(64 + 64 * np.exp(-10.0)))) < 1e-5
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp32_tiny_workload(causal):
+    w = workload("tiny", causal=causal)
+    out = run_gpu(w, DEV)
+    assert out["status"] == 0
+    compare_head(out, w, 0, 0, tol=1e-5, L_tol=1e-6)
+
+
+@pytest.mark.parametrize("N,d,causal", [(1, 16, True), (200, 32, True), (129, 64, False), (300, 128, True)])
+def test_fp32_backward_shapes(N, d, causal):
+    w = workload("tiny", N=N, d=d, causal=causal, B=2, H=2, seed=3).with_(name="fp32_case")
+    gen = torch.Generator().manual_seed(N + d)
+    inputs = tuple(torch.randn(w.B, w.H, N, d, generator=gen) for _ in range(4))
+    out = run_gpu(w, DEV, inputs)
+    assert out["status"] == 0
+    for b in range(w.B):
+        for h in range(w.H):
+            compare_head(out, w, b, h, tol=1e-5, L_tol=1e-6)
+
+
+@pytest.mark.parametrize("N,d,causal", [(1, 64, False), (77, 64, True), (256, 128, False), (1000, 128, True)])
+def test_bf16_forward(N, d, causal):
+    w = workload("causal", B=1, H=2, N=N, d=d, causal=causal, seed=11)
+    q, k, v, _ = (t.to(DEV) for t in make_inputs(w))
+    o, L = fa.attention_forward(q, k, v, w.scale, w.causal)
+    torch.cuda.synchronize()
+    from oracle import attention_forward
+
+    for h in range(2):
+        Or, Lr = attention_forward(to_f64(q[0, h]), to_f64(k[0, h]), to_f64(v[0, h]), w.scale, causal)
+        assert ratio(to_f64(o[0, h]), Or[0, 0]) <= 2e-2
+        assert ratio(to_f64(L[0, h]), Lr[0, 0]) <= 1e-3
+
+
+def test_device_status_stays_clean_and_selftest_times_out():
+    assert fa.get_device_status() == 0
+    fa.selftest_wait_timeout(5_000_000)  # 5 ms; nothing ever arrives
+    assert fa.get_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.get_device_status() == 0  # reading clears the word
+    # the context is still usable afterwards
+    x = torch.ones(4, device=DEV)
+    assert x.sum().item() == 4.0
