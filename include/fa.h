@@ -124,6 +124,22 @@ fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const v
                       const void* O, const void* dO, const float* L, float* D,
                       float* dQ_accum, void* dQ, void* dK, void* dV, void* stream);
 
+/* fa_backward without caller-supplied scratch, for callers that cannot
+ * allocate device memory (a host framework or plugin that owns all device
+ * memory and forbids allocation while it runs, a process with a device-memory
+ * budget fixed at start-up, or a loop that cannot afford cudaMalloc's implicit
+ * synchronisation).  The paper has no counterpart; this is a deployment
+ * convenience.  D and the dQ accumulator live in fixed arrays inside the
+ * library (64 MiB accumulator, 4 MiB D; every GPU that loads the library
+ * holds them until exit).  Problems with fa_dq_accum_elems(p) > 16 Mi floats
+ * or B*H*N > 1 Mi rows return FA_ERR_UNSUPPORTED.  The first call on a device
+ * looks up the arrays' device addresses (make it before any stream capture).
+ * All calls share the arrays: calls that overlap on the GPU race, so order
+ * them on one stream.  Allocates nothing. */
+fa_status fa_backward_static_workspace(const fa_problem* p, const void* Q, const void* K, const void* V,
+                                       const void* O, const void* dO, const float* L, void* dQ, void* dK,
+                                       void* dV, void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  *code receives FA_OK or the first device-side error recorded since
  * the last read.  Returns FA_ERR_CUDA if the synchronisation fails. */
