@@ -178,10 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // work item: key block kb of head (b, h); key block 0 first (longest walk)
-  const int BH = prm.B * prm.H;
-  const int kb = blockIdx.x / BH;
-  const int bh = blockIdx.x % BH;
+  // work item: key block kb of head (b, h).  Heads are walked one after the
+  // other so the CTAs resident at any time share a few heads' Q, dO and dQ
+  // accumulator in L2; inside a head, key block 0 (the longest causal walk)
+  // comes first.
+  const int kb = blockIdx.x % prm.n_tiles;
+  const int bh = blockIdx.x / prm.n_tiles;
   const int b = bh / prm.H, h = bh % prm.H;
   const int k0 = kb * kBlk;
   const int q_first = prm.causal ? kb : 0;
@@ -209,6 +211,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tma_load_4d(sV + c * Ly::kChunk, &tmV, bar(KV_FULL), c * 64, k0, h, b);
       }
     }
+    // L and D rows of the next query block are read into registers one block
+    // ahead, so their global-load latency hides behind the wait for a free
+    // stage.
+    float lv[kBlk / 32], dv[kBlk / 32];
+    auto fetch_rows = [&](int it) {
+      const int q0 = (q_first + it) * kBlk;
+#pragma unroll
+      for (int u = 0; u < kBlk / 32; ++u) {
+        const int q = q0 + lane + 32 * u;
+        lv[u] = q < prm.N ? __ldg(prm.L + (int64_t)bh * prm.N + q) * kLog2e : INFINITY;
+        dv[u] = q < prm.N ? __ldg(prm.D + (int64_t)bh * prm.N + q) : 0.f;
+      }
+    };
+    fetch_rows(0);
     for (int i = 0; i < n_iter; ++i) {
       const int st = i & 1;
       if (i >= 2) {
@@ -218,10 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = (q_first + i) * kBlk;
       float* sL = reinterpret_cast<float*>(smem + Ly::kL) + st * kBlk;
       float* sD = reinterpret_cast<float*>(smem + Ly::kD) + st * kBlk;
-      for (int r = lane; r < kBlk; r += 32) {
-        const int q = q0 + r;
-        sL[r] = q < prm.N ? prm.L[(int64_t)bh * prm.N + q] * kLog2e : INFINITY;
-        sD[r] = q < prm.N ? prm.D[(int64_t)bh * prm.N + q] : 0.f;
+#pragma unroll
+      for (int u = 0; u < kBlk / 32; ++u) {
+        sL[lane + 32 * u] = lv[u];
+        sD[lane + 32 * u] = dv[u];
       }
       __syncwarp();
       if (lane == 0) {
@@ -235,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(bar(FULL0 + st));
       }
       issued = i + 1;
+      if (i + 1 < n_iter) fetch_rows(i + 1);
     }
     if (!ok) {  // let every copy this CTA started land before the CTA exits
       ptx::wait_bounded(bar(KV_FULL), 0, W, false);
@@ -243,59 +260,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
-      constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t kIdKV = ptx::idesc_bf16_f32(128, HD, false, true);   // dV, dK
-      constexpr uint32_t kIdQ = ptx::idesc_bf16_f32(128, HD, true, true);     // dQ
-      // K-major operand: 16-element K step kk inside 64-column chunks
-      auto kdesc = [&](uint32_t tile, int kk) -> uint64_t {
-        return ptx::sdesc_sw128(tile + (kk >> 2) * Ly::kChunk + (kk & 3) * 32, 16, 1024);
-      };
-      // MN-major operand: 16-row K step kk; 64-column MN blocks one chunk apart
-      auto mndesc = [&](uint32_t tile, int kk) -> uint64_t {
-        return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
-      };
-      const uint32_t tS = tmem + Ly::kColS, tP = tmem + Ly::kColP, tdP = tmem + Ly::kColdP;
-      const uint32_t tdQ = tmem + Ly::kColdQ, tdV = tmem + Ly::kColdV, tdK = tmem + Ly::kColdK;
-
-      bool ok = ptx::wait_bounded(bar(KV_FULL), 0, W, true) && ptx::wait_bounded(bar(FULL0), 0, W, true);
-      if (ok) {
-        ptx::tc_fence_after();
+    // The whole warp runs this loop and waits; one elected lane issues the
+    // MMAs and commits.  Every operand is warp-uniform (the TMEM base is
+    // broadcast from lane 0, K steps are unrolled) so each tcgen05.mma issues
+    // at the tensor pipe's own rate.
+    constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+    constexpr uint32_t kIdKV = ptx::idesc_bf16_f32(128, HD, false, true);   // dV, dK
+    constexpr uint32_t kIdQ = ptx::idesc_bf16_f32(128, HD, true, true);     // dQ
+    // K-major operand: 16-element K step kk inside 64-column chunks
+    auto kdesc = [&](uint32_t tile, int kk) -> uint64_t {
+      return ptx::sdesc_sw128(tile + (kk >> 2) * Ly::kChunk + (kk & 3) * 32, 16, 1024);
+    };
+    // MN-major operand: 16-row K step kk; 64-column MN blocks one chunk apart
+    auto mndesc = [&](uint32_t tile, int kk) -> uint64_t {
+      return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
+    };
+    const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+    const uint32_t tS = tm + Ly::kColS, tP = tm + Ly::kColP, tdP = tm + Ly::kColdP;
+    const uint32_t tdQ = tm + Ly::kColdQ, tdV = tm + Ly::kColdV, tdK = tm + Ly::kColdK;
+    auto issue_S = [&](int st) {
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS, kdesc(sK, kk), kdesc(sQ(0), kk), kIdS, kk > 0);
-        ptx::tc_commit(bar(S_FULL));
-      }
-      for (int i = 0; ok && i < n_iter; ++i) {
-        const int st = i & 1;
-        const uint32_t ph = i & 1;
-        // dV += P^T dO   (A = P^T from TMEM)
-        if (!(ok = ptx::wait_bounded(bar(P_FULL), ph, W, true))) break;
-        ptx::tc_fence_after();
+      for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS, kdesc(sK, kk), kdesc(sQ(st), kk), kIdS, kk > 0);
+      ptx::tc_commit(bar(S_FULL));
+    };
+
+    bool ok = warp_wait(bar(KV_FULL), 0, W) && warp_wait(bar(FULL0), 0, W);
+    if (ok) {
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) issue_S(0);
+      __syncwarp();
+    }
+    for (int i = 0; ok && i < n_iter; ++i) {
+      const int st = i & 1;
+      const uint32_t ph = i & 1;
+      // dV += P^T dO   (A = P^T from TMEM)
+      if (!(ok = warp_wait(bar(P_FULL), ph, W))) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
           ptx::mma_ts(tdV, tP + kk * 8, mndesc(sdO(st), kk), kIdKV, (i | kk) != 0);
         ptx::tc_commit(bar(DV_DONE));
-        // dP^T = V dO^T  (its columns held dQ(i-1): wait until drained)
-        if (i > 0) {
-          if (!(ok = ptx::wait_bounded(bar(DQ_EMPTY), (i - 1) & 1, W, true))) break;
-          ptx::tc_fence_after();
-        }
+      }
+      __syncwarp();
+      // dP^T = V dO^T  (its columns held dQ(i-1): wait until drained)
+      if (i > 0) {
+        if (!(ok = warp_wait(bar(DQ_EMPTY), (i - 1) & 1, W))) break;
+        ptx::tc_fence_after();
+      }
+      if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tdP, kdesc(sV, kk), kdesc(sdO(st), kk), kIdS, kk > 0);
         ptx::tc_commit(bar(DP_FULL));
-        // S^T(i+1) = K Q(i+1)^T once dV(i) has read P(i)
-        if (i + 1 < n_iter) {
-          if (!(ok = ptx::wait_bounded(bar(FULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W, true))) break;
-          if (!(ok = ptx::wait_bounded(bar(DV_DONE), ph, W, true))) break;
-          ptx::tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            ptx::mma_ss(tS, kdesc(sK, kk), kdesc(sQ(st ^ 1), kk), kIdS, kk > 0);
-          ptx::tc_commit(bar(S_FULL));
-        }
-        // dK += dS^T Q ;  dQ = dS K
-        if (!(ok = ptx::wait_bounded(bar(DS_FULL), ph, W, true))) break;
+      }
+      __syncwarp();
+      // S^T(i+1) = K Q(i+1)^T once dV(i) has read P(i)
+      if (i + 1 < n_iter) {
+        if (!(ok = warp_wait(bar(FULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W))) break;
+        if (!(ok = warp_wait(bar(DV_DONE), ph, W))) break;
         ptx::tc_fence_after();
+        if (ptx::elect_one()) issue_S(st ^ 1);
+        __syncwarp();
+      }
+      // dK += dS^T Q ;  dQ = dS K
+      if (!(ok = warp_wait(bar(DS_FULL), ph, W))) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
           ptx::mma_ss(tdK, kdesc(sdS, kk), mndesc(sQ(st), kk), kIdKV, (i | kk) != 0);
@@ -304,10 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit(bar(DQ_FULL));
         ptx::tc_commit(bar(EMPTY0 + st));
       }
-      ptx::tc_commit(bar(ACC_FULL));
-      if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
+      __syncwarp();
     }
+    if (ptx::elect_one()) ptx::tc_commit(bar(ACC_FULL));
     __syncwarp();
+    if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
   } else if (warp < 4) {
     // ------------------------------------------------------------ softmax / dS
     const int t = threadIdx.x;  // key row within the block == TMEM lane
