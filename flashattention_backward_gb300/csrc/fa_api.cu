@@ -10,6 +10,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "dq_layout.cuh"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -146,7 +147,7 @@ cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO
 }
 
 // ----------------------------------------------------------------------------
-// Convert: dQ = T(scale * dq_accum), undoing the tile-blocked layout.  One
+// Convert: dQ = T(scale * dq_accum), undoing the unit-blocked layout.  One
 // block per (b, h, 128-row tile): a coalesced read of the tile into shared
 // memory (row-major, padded), then row-contiguous 16-byte output stores.
 // ----------------------------------------------------------------------------
@@ -174,13 +175,14 @@ __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict
   const int tile = blockIdx.x % tiles_per_head;
   const int bh = blockIdx.x / tiles_per_head;
   const int b = bh / H, h = bh % H;
-  const float4* src = reinterpret_cast<const float4*>(acc + ((int64_t)bh * tiles_per_head + tile) * (int64_t)kTileRows * HD);
-  // layout inside a tile: [c/4][row][4]
+  const float4* src = reinterpret_cast<const float4*>(acc + dq_unit_offset(bh, tiles_per_head, tile, 0, 0, HD));
+  // a tile is 4 x (HD/16) units of [4 column groups][32 rows][4 columns]
 #pragma unroll 4
   for (int k = threadIdx.x; k < kTileRows * HD / 4; k += 256) {
-    const int g = k / kTileRows, r = k % kTileRows;
+    const int unit = k / 128, g = (k % 128) / 32, r = k % 32;
+    const int row = (unit / (HD / 16)) * 32 + r, col = (unit % (HD / 16)) * 16 + g * 4;
     const float4 v = __ldg(src + k);
-    *reinterpret_cast<float4*>(tile_s + r * kPitch + g * 4) = v;
+    *reinterpret_cast<float4*>(tile_s + row * kPitch + col) = v;
   }
   __syncthreads();
   constexpr int kVec = 16 / sizeof(T);           // outputs per 16-byte store

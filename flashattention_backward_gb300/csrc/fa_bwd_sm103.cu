@@ -5,38 +5,42 @@
 // Loop order follows "CUDA 算子工程" ch.16 §16.2: one CTA owns a 128-row key
 // block K_j, V_j (resident in shared memory) and walks the 128-row query
 // blocks Q_i, dO_i.  dV_j and dK_j accumulate in tensor memory and are
-// written once; dQ partials leave through fire-and-forget fp32 vector
-// reductions into the tile-blocked accumulator (§16.3, scheme A').  Under the
-// causal mask the walk starts at the diagonal block, so fully masked pairs
-// are never loaded (§16.8 item 2).
+// written once; dQ partials are added into the fp32 accumulator without
+// waiting for the result (§16.3, scheme A'), here by bulk reductions that the
+// TMA unit performs from shared memory.  Under the causal mask the walk starts
+// at the diagonal block, so fully masked pairs are never loaded (§16.8 item 2).
 //
 // The scores are computed transposed, S^T = K_j Q_i^T, so that TMEM lane r is
 // key row r: P^T and dS^T then sit with keys as the M dimension, which is
-// what dV += P^T dO and dK += dS^T Q need, and P^T can feed the dV product
+// what dV += P^T dO and dK += dS^T Q need, and P^T feeds the dV product
 // straight from tensor memory.
 //
 // Warp roles (320 threads):
-//   warps 0-3  "softmax": one thread per key row.  P = exp2(S*scale*log2e -
-//              L*log2e) -> bf16 into TMEM; dS = P * (dP - D) -> bf16 into
-//              shared memory (128-byte swizzle).  Epilogue: dV.
-//   warps 4-7  "dQ": drain the dQ tile from TMEM, reduce into global memory.
-//              Epilogue: dK * scale.
-//   warp  8    TMA producer (K, V once; Q, dO double-buffered) and the L, D
-//              rows of each query block.
-//   warp  9    TMEM allocator; lane 0 issues every MMA.
+//   warps 0-7  compute.  Warp w owns TMEM lanes 32*(w%4) .. +31 (key rows for
+//              S, dP, dV, dK; query rows for dQ) and column half w/4 of them.
+//              Per query block: P = exp2(S*scale*log2e - L*log2e) -> bf16
+//              into TMEM; dQ of the previous block TMEM -> shared memory ->
+//              bulk reduction into global; dS = P * (dP - D) -> bf16 into
+//              shared memory (128-byte swizzle).  Epilogue: dV (w < 4) and
+//              scale * dK (w >= 4).
+//   warp  8    TMA producer: K, V once; Q (two stages, with its L and D rows)
+//              and dO (one stage for d = 128, two for d = 64).
+//   warp  9    TMEM allocator and MMA issuer (one elected lane issues).
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
-//   [0,128)    S^T, then P^T (bf16, columns [0,64)) written over it
-//   [128,256)  dP^T, then the dQ tile of the same step written over it
+//   [0,128)     S^T; P^T (bf16) is written over it: query columns [0,64) of
+//               S become P columns [0,32), [64,128) become [64,96)
+//   [128,256)   dP^T, then the dQ tile of the same step written over it
 //   [256,256+d) dV accumulator, [256+d,256+2d) dK accumulator
 //
 // MMA issue order per query block i (software pipelined):
 //   dV(i)  dP(i)  S(i+1)  dK(i)  dQ(i)
-// so the tensor pipe works on S(i+1) while the softmax warps turn dP(i) into
+// so the tensor pipe works on S(i+1) while the compute warps turn dP(i) into
 // dS(i), and on dK(i), dQ(i), dV(i+1) while they turn S(i+1) into P(i+1).
 //
 // Every wait is bounded; when one runs out the CTA records FA_ERR_TIMEOUT,
-// drains its own TMA loads and MMAs, frees tensor memory and exits.
+// drains its own TMA loads, MMAs and bulk reductions, frees tensor memory and
+// exits.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -47,6 +51,7 @@
 
 #include <mutex>
 
+#include "dq_layout.cuh"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -55,40 +60,48 @@ namespace {
 
 constexpr int kBlk = 128;  // Br = Bc = 128
 constexpr int kThreads = 320;
+constexpr int kComputeThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum BarId {
   KV_FULL = 0,  // K, V landed
-  FULL0,        // query stage 0 (Q, dO, L, D) landed
-  FULL1,
-  EMPTY0,       // query stage 0 free again
-  EMPTY1,
+  QFULL0,       // Q stage (with its L, D rows) landed; 32 arrivals
+  QFULL1,
+  QEMPTY0,      // Q stage free again
+  QEMPTY1,
+  DOFULL0,      // dO stage landed
+  DOFULL1,
+  DOEMPTY0,     // dO stage free again
+  DOEMPTY1,
   S_FULL,       // S^T(i) in TMEM
-  P_FULL,       // P^T(i) in TMEM (128 arrivals)
+  P_FULL,       // P^T(i) in TMEM (256 arrivals)
   DV_DONE,      // dV(i) product done: S/P columns reusable
   DP_FULL,      // dP^T(i) in TMEM
-  DS_FULL,      // dS^T(i) in shared memory (128 arrivals)
-  DQ_FULL,      // dQ(i) in TMEM and dS(i) consumed
-  DQ_EMPTY,     // dQ(i) drained from TMEM (128 arrivals)
+  DS_FULL,      // dS^T(i) in shared memory (256 arrivals)
+  DQ_FULL,      // dQ(i) in TMEM; dS(i) and Q(i) consumed
+  DQ_EMPTY,     // dQ(i) drained from TMEM (256 arrivals)
   ACC_FULL,     // every MMA done: dK, dV final
   kNumBars
 };
 
 template <int HD>
 struct Layout {
+  static constexpr int kDoStages = HD == 128 ? 1 : 2;
   static constexpr int kChunk = kBlk * 128;     // 128 rows x 128 bytes (64 bf16 columns)
   static constexpr int kTile = kBlk * HD * 2;   // one Q / K / V / dO tile
+  static constexpr int kSlot = 4096;            // per compute warp: 2 x 2 KB dQ staging
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;         // 2 stages
-  static constexpr int kdO = kQ + 2 * kTile;    // 2 stages
-  static constexpr int kdS = kdO + 2 * kTile;   // 128 x 128 bf16, two 64-column chunks
-  static constexpr int kL = kdS + 2 * kChunk;   // 2 stages x 128 fp32 (L * log2 e)
-  static constexpr int kD = kL + 2 * kBlk * 4;  // 2 stages x 128 fp32
+  static constexpr int kQ = kV + kTile;                 // 2 stages
+  static constexpr int kdO = kQ + 2 * kTile;            // kDoStages stages
+  static constexpr int kdS = kdO + kDoStages * kTile;   // 128 x 128 bf16, two 64-column chunks
+  static constexpr int kStage = kdS + 2 * kChunk;       // 8 x kSlot
+  static constexpr int kL = kStage + 8 * kSlot;         // 2 stages x 128 fp32 (L * log2 e)
+  static constexpr int kD = kL + 2 * kBlk * 4;          // 2 stages x 128 fp32
   static constexpr int kBar = kD + 2 * kBlk * 4;
-  static constexpr int kMisc = kBar + kNumBars * 8;  // TMEM base address, abort flag
+  static constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
   static constexpr int kBytes = kMisc + 16;
-  static constexpr uint32_t kColS = 0, kColP = 0, kColdP = 128, kColdQ = 128;
+  static constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 128;
   static constexpr uint32_t kColdV = 256, kColdK = 256 + HD;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -141,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                      const BwdParams prm) {
   using Ly = Layout<HD>;
+  constexpr int kDoSt = Ly::kDoStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_addr(smem);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -154,17 +168,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(KV_FULL), 1);
-    ptx::mbar_init(bar(FULL0), 32);
-    ptx::mbar_init(bar(FULL1), 32);
-    ptx::mbar_init(bar(EMPTY0), 1);
-    ptx::mbar_init(bar(EMPTY1), 1);
+    ptx::mbar_init(bar(QFULL0), 32);
+    ptx::mbar_init(bar(QFULL1), 32);
+    ptx::mbar_init(bar(QEMPTY0), 1);
+    ptx::mbar_init(bar(QEMPTY1), 1);
+    ptx::mbar_init(bar(DOFULL0), 1);
+    ptx::mbar_init(bar(DOFULL1), 1);
+    ptx::mbar_init(bar(DOEMPTY0), 1);
+    ptx::mbar_init(bar(DOEMPTY1), 1);
     ptx::mbar_init(bar(S_FULL), 1);
-    ptx::mbar_init(bar(P_FULL), 128);
+    ptx::mbar_init(bar(P_FULL), kComputeThreads);
     ptx::mbar_init(bar(DV_DONE), 1);
     ptx::mbar_init(bar(DP_FULL), 1);
-    ptx::mbar_init(bar(DS_FULL), 128);
+    ptx::mbar_init(bar(DS_FULL), kComputeThreads);
     ptx::mbar_init(bar(DQ_FULL), 1);
-    ptx::mbar_init(bar(DQ_EMPTY), 128);
+    ptx::mbar_init(bar(DQ_EMPTY), kComputeThreads);
     ptx::mbar_init(bar(ACC_FULL), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -176,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tm = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
   // work item: key block kb of head (b, h).  Heads are walked one after the
   // other so the CTAs resident at any time share a few heads' Q, dO and dQ
@@ -198,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     bool ok = true;
-    int issued = 0;
+    int q_issued = 0, do_issued = 0;
     if (lane == 0) {
       ptx::prefetch_tensormap(&tmQ);
       ptx::prefetch_tensormap(&tmK);
@@ -212,8 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // L and D rows of the next query block are read into registers one block
-    // ahead, so their global-load latency hides behind the wait for a free
-    // stage.
+    // ahead, so their global-load latency hides behind the stage waits.
     float lv[kBlk / 32], dv[kBlk / 32];
     auto fetch_rows = [&](int it) {
       const int q0 = (q_first + it) * kBlk;
@@ -227,11 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     fetch_rows(0);
     for (int i = 0; i < n_iter; ++i) {
       const int st = i & 1;
+      const int q0 = (q_first + i) * kBlk;
       if (i >= 2) {
-        ok = warp_wait(bar(EMPTY0 + st), ((i - 2) >> 1) & 1, W);
+        ok = warp_wait(bar(QEMPTY0 + st), ((i - 2) >> 1) & 1, W);
         if (!ok) break;
       }
-      const int q0 = (q_first + i) * kBlk;
       float* sL = reinterpret_cast<float*>(smem + Ly::kL) + st * kBlk;
       float* sD = reinterpret_cast<float*>(smem + Ly::kD) + st * kBlk;
 #pragma unroll
@@ -241,22 +258,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(FULL0 + st), 2 * Ly::kTile);
+        ptx::mbar_arrive_expect_tx(bar(QFULL0 + st), Ly::kTile);
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) {
-          ptx::tma_load_4d(sQ(st) + c * Ly::kChunk, &tmQ, bar(FULL0 + st), c * 64, q0, h, b);
-          ptx::tma_load_4d(sdO(st) + c * Ly::kChunk, &tmdO, bar(FULL0 + st), c * 64, q0, h, b);
-        }
+        for (int c = 0; c < HD / 64; ++c)
+          ptx::tma_load_4d(sQ(st) + c * Ly::kChunk, &tmQ, bar(QFULL0 + st), c * 64, q0, h, b);
       } else {
-        ptx::mbar_arrive(bar(FULL0 + st));
+        ptx::mbar_arrive(bar(QFULL0 + st));
       }
-      issued = i + 1;
+      q_issued = i + 1;
+      const int sd = i % kDoSt;
+      if (i >= kDoSt) {
+        ok = warp_wait(bar(DOEMPTY0 + sd), ((i - kDoSt) / kDoSt) & 1, W);
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(DOFULL0 + sd), Ly::kTile);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c)
+          ptx::tma_load_4d(sdO(sd) + c * Ly::kChunk, &tmdO, bar(DOFULL0 + sd), c * 64, q0, h, b);
+      }
+      __syncwarp();
+      do_issued = i + 1;
       if (i + 1 < n_iter) fetch_rows(i + 1);
     }
     if (!ok) {  // let every copy this CTA started land before the CTA exits
       ptx::wait_bounded(bar(KV_FULL), 0, W, false);
-      for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-        ptx::wait_bounded(bar(FULL0 + (i & 1)), (i >> 1) & 1, W, false);
+      for (int i = q_issued > 2 ? q_issued - 2 : 0; i < q_issued; ++i)
+        ptx::wait_bounded(bar(QFULL0 + (i & 1)), (i >> 1) & 1, W, false);
+      for (int i = do_issued > kDoSt ? do_issued - kDoSt : 0; i < do_issued; ++i)
+        ptx::wait_bounded(bar(DOFULL0 + i % kDoSt), (i / kDoSt) & 1, W, false);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
@@ -275,8 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto mndesc = [&](uint32_t tile, int kk) -> uint64_t {
       return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
     };
-    const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
-    const uint32_t tS = tm + Ly::kColS, tP = tm + Ly::kColP, tdP = tm + Ly::kColdP;
+    const uint32_t tS = tm + Ly::kColS, tdP = tm + Ly::kColdP;
     const uint32_t tdQ = tm + Ly::kColdQ, tdV = tm + Ly::kColdV, tdK = tm + Ly::kColdK;
     auto issue_S = [&](int st) {
 #pragma unroll
@@ -284,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_commit(bar(S_FULL));
     };
 
-    bool ok = warp_wait(bar(KV_FULL), 0, W) && warp_wait(bar(FULL0), 0, W);
+    bool ok = warp_wait(bar(KV_FULL), 0, W) && warp_wait(bar(QFULL0), 0, W);
     if (ok) {
       ptx::tc_fence_after();
       if (ptx::elect_one()) issue_S(0);
@@ -292,14 +321,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; ok && i < n_iter; ++i) {
       const int st = i & 1;
+      const int sd = i % kDoSt;
       const uint32_t ph = i & 1;
-      // dV += P^T dO   (A = P^T from TMEM)
+      // dV += P^T dO   (A = P^T from TMEM: query k-steps 0-3 in columns
+      // [0,32), 4-7 in [64,96))
       if (!(ok = warp_wait(bar(P_FULL), ph, W))) break;
+      if (!(ok = warp_wait(bar(DOFULL0 + sd), (i / kDoSt) & 1, W))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          ptx::mma_ts(tdV, tP + kk * 8, mndesc(sdO(st), kk), kIdKV, (i | kk) != 0);
+          ptx::mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
         ptx::tc_commit(bar(DV_DONE));
       }
       __syncwarp();
@@ -310,13 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tdP, kdesc(sV, kk), kdesc(sdO(st), kk), kIdS, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tdP, kdesc(sV, kk), kdesc(sdO(sd), kk), kIdS, kk > 0);
         ptx::tc_commit(bar(DP_FULL));
+        ptx::tc_commit(bar(DOEMPTY0 + sd));
       }
       __syncwarp();
       // S^T(i+1) = K Q(i+1)^T once dV(i) has read P(i)
       if (i + 1 < n_iter) {
-        if (!(ok = warp_wait(bar(FULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W))) break;
+        if (!(ok = warp_wait(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W))) break;
         if (!(ok = warp_wait(bar(DV_DONE), ph, W))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) issue_S(st ^ 1);
@@ -332,76 +365,120 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk) ptx::mma_ss(tdQ, mndesc(sdS, kk), mndesc(sK, kk), kIdQ, kk > 0);
         ptx::tc_commit(bar(DQ_FULL));
-        ptx::tc_commit(bar(EMPTY0 + st));
+        ptx::tc_commit(bar(QEMPTY0 + st));
       }
       __syncwarp();
     }
     if (ptx::elect_one()) ptx::tc_commit(bar(ACC_FULL));
     __syncwarp();
     if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ softmax / dS
-    const int t = threadIdx.x;  // key row within the block == TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int kr = k0 + t;
+  } else {
+    // ------------------------------------------------------------ compute
+    const int qq = warp & 3;               // TMEM lane quarter
+    const int G = warp >> 2;               // column half
+    const int t = qq * 32 + lane;          // TMEM lane
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    const int kr = k0 + t;                 // key row of S, dP, dV, dK
     const bool key_ok = kr < prm.N;
     const float sl2 = prm.scale * kLog2e;
+    const int c0 = G * 64;                 // query columns [c0, c0 + 64) of S, dP
+    const uint32_t slot = sbase + Ly::kStage + warp * Ly::kSlot;
+    int rounds = 0;                        // dQ staging rounds issued by this warp
+    uint32_t pk[32];                       // P for columns c0 .. c0 + 63, bf16 pairs
+
+    // dQ(it): TMEM -> registers (then the TMEM columns are released) ->
+    // shared memory in 2 KB units -> bulk reduction into the accumulator.
+    // The two halves of the warp's slot alternate, so a unit is written while
+    // the previous one is still being read by the TMA unit.
+    auto drain_dq = [&](int it) -> bool {
+      if (!warp_wait(bar(DQ_FULL), it & 1, W)) return false;
+      ptx::tc_fence_after();
+      constexpr int kCols = HD / 2;        // this warp's dQ columns [G * kCols, +kCols)
+      uint32_t r[kCols];
+      if constexpr (kCols == 64) {
+        ptx::tmem_ld64(tm + Ly::kColdQ + lane_off + G * 64, tm + Ly::kColdQ + lane_off + G * 64 + 32,
+                       *reinterpret_cast<uint32_t(*)[64]>(r));
+      } else {
+        ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(r));
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(DQ_EMPTY));
+      float* unit0 = prm.dq_accum + dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * (kCols / 16), HD);
+#pragma unroll
+      for (int u = 0; u < kCols / 16; ++u) {
+        const uint32_t half = slot + (rounds & 1) * 2048;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          ptx::st_shared_v4(half + g * 512 + lane * 16, r[u * 16 + 4 * g], r[u * 16 + 4 * g + 1],
+                            r[u * 16 + 4 * g + 2], r[u * 16 + 4 * g + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::bulk_reduce_add_f32(unit0 + u * kDqUnitFloats, half, kDqUnitFloats * 4);
+          ptx::bulk_commit();
+        }
+        ++rounds;
+      }
+      return true;
+    };
+
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
       const int st = i & 1;
       const uint32_t ph = i & 1;
       const int q0 = (q_first + i) * kBlk;
+      // ---- P(i)
       if (!(ok = warp_wait(bar(S_FULL), ph, W))) break;
-      if (!(ok = warp_wait(bar(FULL0 + st), (i >> 1) & 1, W))) break;
+      if (!(ok = warp_wait(bar(QFULL0 + st), (i >> 1) & 1, W))) break;
       ptx::tc_fence_after();
-      const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4;
-      const bool diag = prm.causal && q0 == k0;
-      uint32_t pk[64];
+      {
+        uint32_t r[64];
+        ptx::tmem_ld64(tm + Ly::kColS + lane_off + c0, tm + Ly::kColS + lane_off + c0 + 32, r);
+        const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4 + c0 * 4;
+        const bool diag = prm.causal && q0 == k0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tmem + Ly::kColS + lane_off + c * 32, r);
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const int col = c * 32 + j;
-          const float4 l4 = ptx::ld_shared_f4(sLa + col * 4);
+        for (int j = 0; j < 64; j += 4) {
+          const float4 l4 = ptx::ld_shared_f4(sLa + j * 4);
           float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
           float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
           float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
           float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
           if (diag) {  // key k0 + t is visible to query q0 + col iff t <= col
+            const int col = c0 + j;
             p0 = col + 0 < t ? 0.f : p0;
             p1 = col + 1 < t ? 0.f : p1;
             p2 = col + 2 < t ? 0.f : p2;
             p3 = col + 3 < t ? 0.f : p3;
           }
-          pk[c * 16 + j / 2] = ptx::pack_bf16x2(p0, p1);
-          pk[c * 16 + j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+          pk[j / 2] = ptx::pack_bf16x2(p0, p1);
+          pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
         }
-      }
-      if (!key_ok) {
+        if (!key_ok) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) pk[k] = 0u;
+          for (int k = 0; k < 32; ++k) pk[k] = 0u;
+        }
+        ptx::tmem_st16(tm + Ly::kColS + lane_off + G * 64, &pk[0]);
+        ptx::tmem_st16(tm + Ly::kColS + lane_off + G * 64 + 16, &pk[16]);
+        ptx::tmem_st_wait();
       }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_st16(tmem + Ly::kColP + lane_off + c * 16, &pk[c * 16]);
-      ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(P_FULL));
-
+      // ---- dQ(i-1); also guarantees dS(i-1) has been consumed
+      if (i > 0 && !(ok = drain_dq(i - 1))) break;
+      // ---- dS(i)
       if (!(ok = warp_wait(bar(DP_FULL), ph, W))) break;
-      if (i > 0 && !(ok = warp_wait(bar(DQ_FULL), (i - 1) & 1, W))) break;  // dS(i-1) consumed
       ptx::tc_fence_after();
-      const uint32_t sDa = sbase + Ly::kD + st * kBlk * 4;
+      {
+        uint32_t r[64];
+        ptx::tmem_ld64(tm + Ly::kColdP + lane_off + c0, tm + Ly::kColdP + lane_off + c0 + 32, r);
+        const uint32_t sDa = sbase + Ly::kD + st * kBlk * 4 + c0 * 4;
+        uint32_t ds[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tmem + Ly::kColdP + lane_off + c * 32, r);
-        uint32_t ds[16];
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 d4 = ptx::ld_shared_f4(sDa + (c * 32 + j) * 4);
-          const uint32_t pa = pk[c * 16 + j / 2], pb = pk[c * 16 + j / 2 + 1];
+        for (int j = 0; j < 64; j += 4) {
+          const float4 d4 = ptx::ld_shared_f4(sDa + j * 4);
+          const uint32_t pa = pk[j / 2], pb = pk[j / 2 + 1];
           const float ds0 = ptx::bf16lo(pa) * (__uint_as_float(r[j + 0]) - d4.x);
           const float ds1 = ptx::bf16hi(pa) * (__uint_as_float(r[j + 1]) - d4.y);
           const float ds2 = ptx::bf16lo(pb) * (__uint_as_float(r[j + 2]) - d4.z);
@@ -409,49 +486,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           ds[j / 2] = ptx::pack_bf16x2(ds0, ds1);
           ds[j / 2 + 1] = ptx::pack_bf16x2(ds2, ds3);
         }
-        // row t of dS^T, query columns [32c, 32c + 32): 4 x 16-byte pieces,
-        // 128-byte swizzle (piece index XOR row % 8)
-        const uint32_t row = sdS + (c >> 1) * Ly::kChunk + t * 128;
+        // row t of dS^T, query columns [c0, c0 + 64) = chunk G: eight 16-byte
+        // pieces, 128-byte swizzle (piece index XOR row % 8)
+        const uint32_t row = sdS + G * Ly::kChunk + t * 128;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t piece = (uint32_t)((c & 1) * 4 + u);
-          ptx::st_shared_v4(row + ((piece ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1], ds[4 * u + 2],
-                            ds[4 * u + 3]);
-        }
+        for (int u = 0; u < 8; ++u)
+          ptx::st_shared_v4(row + (((uint32_t)u ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1],
+                            ds[4 * u + 2], ds[4 * u + 3]);
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DS_FULL));
     }
+    if (ok && n_iter > 0) ok = drain_dq(n_iter - 1);
+    if (lane == 0) ptx::bulk_wait_all();  // this warp's reductions are complete
+    __syncwarp();
     if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
       ptx::tc_fence_after();
-      store_row<HD>(tmem + Ly::kColdV + lane_off, key_ok, prm.dV + head + (int64_t)kr * prm.sn, 1.0f);
-    }
-  } else {
-    // ------------------------------------------------------------ dQ drain
-    const int t = threadIdx.x - 128;  // query row within the block == TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    bool ok = true;
-    for (int i = 0; i < n_iter; ++i) {
-      if (!(ok = warp_wait(bar(DQ_FULL), i & 1, W))) break;
-      ptx::tc_fence_after();
-      uint32_t r[HD];
-#pragma unroll
-      for (int c = 0; c < HD / 32; ++c)
-        ptx::tmem_ld32(tmem + Ly::kColdQ + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(DQ_EMPTY));
-      const int qt = q_first + i;
-      float* base = prm.dq_accum + ((int64_t)bh * prm.n_tiles + qt) * (int64_t)(kBlk * HD) + t * 4;
-#pragma unroll
-      for (int g = 0; g < HD / 4; ++g)
-        ptx::red_add_v4(base + g * (kBlk * 4), __uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                        __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
-    }
-    const int kr = k0 + t;
-    if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
-      ptx::tc_fence_after();
-      store_row<HD>(tmem + Ly::kColdK + lane_off, kr < prm.N, prm.dK + head + (int64_t)kr * prm.sn, prm.scale);
+      if (G == 0)
+        store_row<HD>(tm + Ly::kColdV + lane_off, key_ok, prm.dV + head + (int64_t)kr * prm.sn, 1.0f);
+      else
+        store_row<HD>(tm + Ly::kColdK + lane_off, key_ok, prm.dK + head + (int64_t)kr * prm.sn, prm.scale);
     }
   }
 
@@ -459,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 9) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, Ly::kTmemCols);
+    ptx::tmem_dealloc(tm, Ly::kTmemCols);
   }
 }
 

@@ -12,6 +12,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "dq_layout.cuh"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict_
 // ----------------------------------------------------------------------------
 // fp32 backward.  One block per (b, h, 64-key block); inner loop over query
 // tiles.  dV and dK accumulate in registers; dQ partials go to the fp32
-// accumulator with atomicAdd (tile-blocked layout of include/fa.h).
+// accumulator with atomicAdd (unit-blocked layout of include/fa.h).
 // ----------------------------------------------------------------------------
 template <int HD>
 __global__ void __launch_bounds__(kThreads) bwd_simt_fp32_kernel(
@@ -301,11 +302,10 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_fp32_kernel(
     for (int a = 0; a < 4; ++a) {
       const int i = q0 + ty + 16 * a;
       if (i >= N) continue;
-      float* base = dq_accum + ((int64_t)bh * acc_tiles + i / kTileRows) * (int64_t)kTileRows * HD + (i % kTileRows) * 4;
 #pragma unroll
       for (int u = 0; u < kCols; ++u) {
         const int c = tx + 16 * u;
-        atomicAdd(base + (c / 4) * (kTileRows * 4) + (c % 4), dq[a][u]);
+        atomicAdd(dq_accum + dq_accum_index(bh, acc_tiles, i, c, HD), dq[a][u]);
       }
     }
   }

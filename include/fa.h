@@ -48,12 +48,17 @@
  * dQ accumulator layout
  * ---------------------
  * Query rows are grouped into tiles of 128 rows; the last tile of a head is
- * padded to 128 rows.  Element (b, h, n, c) lives at float index
+ * padded to 128 rows.  Inside a tile the rows form 4 quarters of 32 and the
+ * columns blocks of 16; each (quarter, block) pair is a 2 KB unit laid out
+ * [4 column groups of 4][32 rows][4 columns].  Element (b, h, n, c) lives at
+ * float index
  *
- *   ((((b*H + h) * T + n/128) * (d/4) + c/4) * 128 + n%128) * 4 + c%4
+ *   ((((b*H + h) * T + n/128) * 4 + (n%128)/32) * (d/16) + c/16) * 512
+ *     + ((c%16)/4) * 128 + (n%32) * 4 + c%4
  *
- * with T = ceil(N/128), so 32 consecutive rows of one 4-column group are 512
- * contiguous bytes.  Padding rows receive only zero contributions.
+ * with T = ceil(N/128).  One unit is what the tensor-core kernel stages in
+ * shared memory and adds into the accumulator with one bulk reduction.
+ * Padding rows receive only zero contributions.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -107,7 +112,8 @@ fa_status fa_bwd_preprocess(const fa_problem* p, const void* O, const void* dO,
  * for each query block Q_i that the causal mask leaves partly visible:
  *   S = scale Q_i K_j^T, P = exp(S - L_i) (masked entries 0),
  *   dV_j += P^T dO_i,  dP = dO_i V_j^T,  dS = P * (dP - D_i),
- *   dQ_accum[i] += dS K_j  (fire-and-forget float32 reductions, no scale),
+ *   dQ_accum[i] += dS K_j  (float32 reductions the kernel does not wait
+ *                           for; no scale),
  *   dK_j += dS^T Q_i.
  * Writes dV_j and scale * dK_j once per key block.  dQ_accum must hold the
  * zeros written by fa_bwd_preprocess (or earlier partial sums to add to). */

@@ -22,11 +22,12 @@ def _lib():
 
 
 def _accum_index(B, H, N, d):
-    """Float index of element (b, h, n, c) in the tile-blocked accumulator
+    """Float index of element (b, h, n, c) in the unit-blocked accumulator
     layout that include/fa.h documents."""
     T = -(-N // 128)
     b, h, n, c = np.meshgrid(np.arange(B), np.arange(H), np.arange(N), np.arange(d), indexing="ij")
-    return ((((b * H + h) * T + n // 128) * (d // 4) + c // 4) * 128 + n % 128) * 4 + c % 4
+    unit = (((b * H + h) * T + n // 128) * 4 + (n % 128) // 32) * (d // 16) + c // 16
+    return unit * 512 + ((c % 16) // 4) * 128 + (n % 32) * 4 + c % 4
 
 
 @pytest.mark.parametrize("dtype,d,N", [(torch.bfloat16, 64, 300), (torch.bfloat16, 128, 129),
