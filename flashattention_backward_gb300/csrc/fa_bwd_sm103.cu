@@ -6,8 +6,7 @@
 // block K_j, V_j (resident in shared memory) and walks the 128-row query
 // blocks Q_i, dO_i.  dV_j and dK_j accumulate in tensor memory and are
 // written once; dQ partials are added into the fp32 accumulator without
-// waiting for the result (§16.3, scheme A'), here by bulk reductions that the
-// TMA unit performs from shared memory.  Under the causal mask the walk starts
+// waiting for the result (§16.3, scheme A').  Under the causal mask the walk starts
 // at the diagonal block, so fully masked pairs are never loaded (§16.8 item 2).
 //
 // The scores are computed transposed, S^T = K_j Q_i^T, so that TMEM lane r is
@@ -19,10 +18,12 @@
 //   warps 0-7  compute.  Warp w owns TMEM lanes 32*(w%4) .. +31 (key rows for
 //              S, dP, dV, dK; query rows for dQ) and column half w/4 of them.
 //              Per query block: P = exp2(S*scale*log2e - L*log2e) -> bf16
-//              into TMEM; dQ of the previous block TMEM -> shared memory ->
-//              bulk reduction into global; dS = P * (dP - D) -> bf16 into
-//              shared memory (128-byte swizzle).  Epilogue: dV (w < 4) and
-//              scale * dK (w >= 4).
+//              into TMEM; dQ of the previous block TMEM -> registers ->
+//              fp32 reductions into global (vector reductions, or a bulk
+//              reduction through shared memory for the warps that share an
+//              SM sub-partition with the MMA warp); dS = P * (dP - D) -> bf16
+//              into shared memory (128-byte swizzle).  Epilogue: dV (w < 4)
+//              and scale * dK (w >= 4).
 //   warp  8    TMA producer: K, V once; Q (two stages, with its L and D rows)
 //              and dO (one stage for d = 128, two for d = 64).
 //   warp  9    TMEM allocator and MMA issuer (one elected lane issues).
@@ -89,14 +90,13 @@ struct Layout {
   static constexpr int kDoStages = HD == 128 ? 1 : 2;
   static constexpr int kChunk = kBlk * 128;     // 128 rows x 128 bytes (64 bf16 columns)
   static constexpr int kTile = kBlk * HD * 2;   // one Q / K / V / dO tile
-  static constexpr int kSlot = 4096;            // per compute warp: 2 x 2 KB dQ staging
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;                 // 2 stages
   static constexpr int kdO = kQ + 2 * kTile;            // kDoStages stages
   static constexpr int kdS = kdO + kDoStages * kTile;   // 128 x 128 bf16, two 64-column chunks
-  static constexpr int kStage = kdS + 2 * kChunk;       // 8 x kSlot
-  static constexpr int kL = kStage + 8 * kSlot;         // 2 stages x 128 fp32 (L * log2 e)
+  static constexpr int kStage = kdS + 2 * kChunk;       // dQ staging of lane quarter 1: 2 warps x 2 slots
+  static constexpr int kL = kStage + 2 * 2 * (HD / 32) * 2048;  // 2 stages x 128 fp32 (L * log2 e)
   static constexpr int kD = kL + 2 * kBlk * 4;          // 2 stages x 128 fp32
   static constexpr int kBar = kD + 2 * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
@@ -382,18 +382,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool key_ok = kr < prm.N;
     const float sl2 = prm.scale * kLog2e;
     const int c0 = G * 64;                 // query columns [c0, c0 + 64) of S, dP
-    const uint32_t slot = sbase + Ly::kStage + warp * Ly::kSlot;
-    int rounds = 0;                        // dQ staging rounds issued by this warp
+    int rounds = 0;                        // bulk reductions issued by this warp
     uint32_t pk[32];                       // P for columns c0 .. c0 + 63, bf16 pairs
 
-    // dQ(it): TMEM -> registers (then the TMEM columns are released) ->
-    // shared memory in 2 KB units -> bulk reduction into the accumulator.
-    // The two halves of the warp's slot alternate, so a unit is written while
-    // the previous one is still being read by the TMA unit.
+    // dQ(it): TMEM -> registers (then the TMEM columns are released) -> the
+    // accumulator.  Reductions issued on the MMA warp's SM sub-partition
+    // (lane quarter 1) delay its tcgen05.mma issue, so those two warps stage
+    // their share in shared memory and hand it to the TMA unit as one bulk
+    // reduction (two alternating slots per warp); the other six warps issue
+    // vector reductions straight from registers.
     auto drain_dq = [&](int it) -> bool {
       if (!warp_wait(bar(DQ_FULL), it & 1, W)) return false;
       ptx::tc_fence_after();
       constexpr int kCols = HD / 2;        // this warp's dQ columns [G * kCols, +kCols)
+      constexpr int kUnits = kCols / 16;   // 2 KB units, contiguous in the accumulator
       uint32_t r[kCols];
       if constexpr (kCols == 64) {
         ptx::tmem_ld64(tm + Ly::kColdQ + lane_off + G * 64, tm + Ly::kColdQ + lane_off + G * 64 + 32,
@@ -403,23 +405,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DQ_EMPTY));
-      float* unit0 = prm.dq_accum + dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * (kCols / 16), HD);
-#pragma unroll
-      for (int u = 0; u < kCols / 16; ++u) {
-        const uint32_t half = slot + (rounds & 1) * 2048;
+      float* unit0 = prm.dq_accum + dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * kUnits, HD);
+      if (qq == 1) {
+        const uint32_t buf = sbase + Ly::kStage + G * (2 * kUnits * 2048) + (rounds & 1) * (kUnits * 2048);
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         __syncwarp();
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-          ptx::st_shared_v4(half + g * 512 + lane * 16, r[u * 16 + 4 * g], r[u * 16 + 4 * g + 1],
-                            r[u * 16 + 4 * g + 2], r[u * 16 + 4 * g + 3]);
+        for (int u = 0; u < kUnits; ++u)
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            ptx::st_shared_v4(buf + u * 2048 + g * 512 + lane * 16, r[u * 16 + 4 * g], r[u * 16 + 4 * g + 1],
+                              r[u * 16 + 4 * g + 2], r[u * 16 + 4 * g + 3]);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::bulk_reduce_add_f32(unit0 + u * kDqUnitFloats, half, kDqUnitFloats * 4);
+          ptx::bulk_reduce_add_f32(unit0, buf, kUnits * 2048);
           ptx::bulk_commit();
         }
         ++rounds;
+      } else {
+#pragma unroll
+        for (int m = 0; m < kCols / 4; ++m)
+          ptx::red_add_v4(unit0 + (m / 4) * kDqUnitFloats + (m % 4) * 128 + lane * 4, __uint_as_float(r[4 * m]),
+                          __uint_as_float(r[4 * m + 1]), __uint_as_float(r[4 * m + 2]),
+                          __uint_as_float(r[4 * m + 3]));
       }
       return true;
     };
