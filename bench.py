@@ -211,6 +211,7 @@ def main(argv=None) -> int:
     ap.add_argument("--ref-heads", type=int, default=1, help="heads per oracle step (reference arm)")
     ap.add_argument("--cpu-heads", type=int, default=2, help="heads in the cpu_baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-group", type=int, default=0, help="heads per group in the end-to-end leg (0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -304,22 +305,23 @@ def main(argv=None) -> int:
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     cvt_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: fa_backward_host
+    # streams groups of heads through a device workspace, copies overlapped
+    # with compute; every input crosses host->device and every gradient
+    # device->host inside the timed region.
     e2e = None
     if args.e2e_steps > 0:
-        pin = lambda t: t.pin_memory()
+        pin = lambda t: t.contiguous().pin_memory()
         hq, hk, hv, hg = (pin(t) for t in (q_h, k_h, v_h, g_h))
         ho, hL = pin(o.cpu()), pin(L.cpu())
-        hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(3))
+        houts = tuple(torch.empty_like(hq).pin_memory() for _ in range(3))
+        ws = torch.empty(fa.fa_backward_host_workspace_bytes(p, args.e2e_group), dtype=torch.uint8, device=dev)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ho, hg, hL))
-        d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
+        d2h = sum(t.numel() * t.element_size() for t in houts)
 
         def e2e_step():
-            for dst, src in ((q, hq), (k, hk), (v, hv), (o, ho), (g, hg), (L, hL)):
-                dst.copy_(src, non_blocking=True)
-            fa.fa_backward(p, q, k, v, o, g, L, D, acc, dq, dk, dv, stream)
-            for dst, src in ((hdq, dq), (hdk, dk), (hdv, dv)):
-                dst.copy_(src, non_blocking=True)
+            fa.attention_backward_host(hq, hk, hv, ho, hg, hL, w.scale, w.causal, args.e2e_group, workspace=ws,
+                                       out=houts, stream=stream)
 
         for _ in range(3):
             e2e_step()
@@ -336,7 +338,8 @@ def main(argv=None) -> int:
         if fa.get_device_status() != 0:
             raise RuntimeError("device status set during the end-to-end leg")
         e2e = {"value": whole_job_tflops(w.counted_flops, world, args.e2e_steps, e2e_ms), "unit": "TFLOPS",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.e2e_steps,
+               "api": "fa_backward_host (pinned host buffers, %s heads per group)" % (args.e2e_group or "auto")}
 
     peaks, peak_src = load_peaks()
     flops = w.counted_flops

@@ -32,7 +32,10 @@ __all__ = [
     "fa_bwd",
     "fa_convert_dq",
     "fa_backward",
+    "fa_backward_host",
+    "fa_backward_host_workspace_bytes",
     "attention_forward",
+    "attention_backward_host",
     "attention_backward",
     "get_device_status",
     "set_wait_limit_ns",
@@ -95,6 +98,10 @@ def load_library() -> ctypes.CDLL:
     lib.fa_backward.argtypes = [P, vp, vp, vp, vp, vp, fp, fp, fp, vp, vp, vp, vp]
     for name in ("fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_convert_dq", "fa_backward"):
         getattr(lib, name).restype = st
+    lib.fa_backward_host_workspace_bytes.argtypes = [P, ctypes.c_int32]
+    lib.fa_backward_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_backward_host.argtypes = [P] + [vp] * 9 + [vp, ctypes.c_size_t, ctypes.c_int32, vp]
+    lib.fa_backward_host.restype = st
     lib.fa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.fa_get_device_status.restype = st
     lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -234,6 +241,40 @@ def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, st
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fa_backward(p, q, k, v, o, do, L, D, acc, dq, dk, dv, stream)
     return dq, dk, dv
+
+
+def fa_backward_host_workspace_bytes(p: FaProblem, heads_per_group: int = 0) -> int:
+    return int(load_library().fa_backward_host_workspace_bytes(ctypes.byref(p), int(heads_per_group)))
+
+
+def fa_backward_host(p: FaProblem, q, k, v, o, do, L, dq, dk, dv, workspace, heads_per_group: int = 0,
+                     stream=None) -> None:
+    """Backward from host tensors (dense, ideally pinned) through a device
+    workspace; see include/fa.h."""
+    for t in (q, k, v, o, do, dq, dk, dv):
+        if t.is_cuda or not t.is_contiguous() or t.shape != (p.B, p.H, p.N, p.d) or _dtype_code(t) != p.dtype:
+            raise ValueError("host tensors must be dense [B, H, N, d] CPU tensors of the problem dtype")
+    if L.is_cuda or not L.is_contiguous() or L.numel() != p.B * p.H * p.N or L.dtype != torch.float32:
+        raise ValueError("L must be a dense float32 CPU tensor of B*H*N elements")
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be device memory")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load_library().fa_backward_host(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(L),
+                                           _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), nbytes,
+                                           int(heads_per_group), _stream(stream)), "fa_backward_host")
+
+
+def attention_backward_host(q, k, v, o, do, L, scale: float, causal: bool = False, heads_per_group: int = 0,
+                            workspace=None, out=None, stream=None):
+    """dQ, dK, dV (pinned host tensors) for host-resident inputs."""
+    p = problem_for(q, scale, causal)
+    if workspace is None:
+        workspace = torch.empty(fa_backward_host_workspace_bytes(p, heads_per_group), dtype=torch.uint8,
+                                device="cuda")
+    if out is None:
+        out = tuple(torch.empty_like(q).pin_memory() for _ in range(3))
+    fa_backward_host(p, q, k, v, o, do, L, *out, workspace, heads_per_group, stream)
+    return out
 
 
 def get_device_status(stream=None) -> int:

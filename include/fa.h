@@ -130,6 +130,22 @@ fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const v
                       const void* O, const void* dO, const float* L, float* D,
                       float* dQ_accum, void* dQ, void* dK, void* dV, void* stream);
 
+/* Backward pass for tensors in host memory (page-locked for overlap):
+ * Q, K, V, O, dO, dQ, dK, dV dense [B, H, N, d] host arrays (stride_n = d,
+ * stride_h = N*d, stride_b = H*N*d), L a dense [B, H, N] float32 host array.
+ * Heads are independent, so the batch streams through `workspace` (device
+ * memory, 256-byte aligned, at least fa_backward_host_workspace_bytes()) in
+ * groups of `heads_per_group` heads (0: about four groups): group c+1 is
+ * copied in and group c-1 copied out while group c runs fa_backward on
+ * `stream`.  Returns after enqueueing; `stream` continues only once the last
+ * result has reached host memory.  Copies use two library-owned streams
+ * created on first use per device.  No counterpart on the pages: it feeds
+ * the backward from host-resident activations. */
+size_t fa_backward_host_workspace_bytes(const fa_problem* p, int32_t heads_per_group);
+fa_status fa_backward_host(const fa_problem* p, const void* Q, const void* K, const void* V, const void* O,
+                           const void* dO, const float* L, void* dQ, void* dK, void* dV, void* workspace,
+                           size_t workspace_bytes, int32_t heads_per_group, void* stream);
+
 /* fa_backward without caller-supplied scratch, for callers that cannot
  * allocate device memory (a host framework or plugin that owns all device
  * memory and forbids allocation while it runs, a process with a device-memory
