@@ -51,6 +51,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "dq_layout.cuh"
 #include "fa_internal.h"
@@ -382,31 +383,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool key_ok = kr < prm.N;
     const float sl2 = prm.scale * kLog2e;
     const int c0 = G * 64;                 // query columns [c0, c0 + 64) of S, dP
+    constexpr int kCols = HD / 2;          // this warp's dQ columns [G * kCols, +kCols)
+    constexpr int kUnits = kCols / 16;     // 2 KB units, contiguous in the accumulator
+    constexpr int kReds = kCols / 4;       // 16-byte reductions per lane per query block
+    constexpr int kRedsQuarter = kReds / 4;
+    // d = 128: half the reductions ride along with dS(i), half with P(i+1).
+    // d = 64 (half the MMA work per block, eight reductions per lane): they
+    // are issued right after the drain, which measured faster.
+    constexpr bool kSplitReds = HD == 128;
+    // S and dP columns are read from TMEM in halves where reductions ride
+    // along, else in one 64-column load.
+    constexpr int kHalves = kSplitReds ? 2 : 1;
+    constexpr int kW = 64 / kHalves;
+    auto tmem_ld_cols = [&](uint32_t taddr, uint32_t(&r)[kW]) {
+      if constexpr (kW == 64) ptx::tmem_ld64(taddr, taddr + 32, r);
+      else ptx::tmem_ld32(taddr, r);
+    };
+    // Reductions issued on the MMA warp's SM sub-partition (lane quarter 1)
+    // delay its tcgen05.mma issue, so those two warps stage their dQ share in
+    // shared memory and hand it to the TMA unit as one bulk reduction (two
+    // alternating slots per warp).  The other six warps issue vector
+    // reductions from registers; at d = 128 they keep the drained dQ and
+    // issue it in quarters between the halves of the next dS and P
+    // computations, so the load/store unit sees a steady stream instead of a
+    // burst that would stall them.
+    const bool staged = qq == 1;
     int rounds = 0;                        // bulk reductions issued by this warp
     uint32_t pk[32];                       // P for columns c0 .. c0 + 63, bf16 pairs
+    uint32_t dq[kCols];                    // drained dQ of the previous query block
+    float* dq_dst = nullptr;               // its first unit in the accumulator
+    bool pending = false;                  // reductions of dq still to issue
 
-    // dQ(it): TMEM -> registers (then the TMEM columns are released) -> the
-    // accumulator.  Reductions issued on the MMA warp's SM sub-partition
-    // (lane quarter 1) delay its tcgen05.mma issue, so those two warps stage
-    // their share in shared memory and hand it to the TMA unit as one bulk
-    // reduction (two alternating slots per warp); the other six warps issue
-    // vector reductions straight from registers.
+    auto issue_reds = [&](auto m0c) {      // reductions m0 .. m0 + kRedsQuarter - 1
+      constexpr int m0 = decltype(m0c)::value;
+#pragma unroll
+      for (int m = m0; m < m0 + kRedsQuarter; ++m)
+        ptx::red_add_v4(dq_dst + (m / 4) * kDqUnitFloats + (m % 4) * 128 + lane * 4, __uint_as_float(dq[4 * m]),
+                        __uint_as_float(dq[4 * m + 1]), __uint_as_float(dq[4 * m + 2]),
+                        __uint_as_float(dq[4 * m + 3]));
+    };
+    using Q0 = std::integral_constant<int, 0>;
+    using Q1 = std::integral_constant<int, kRedsQuarter>;
+    using Q2 = std::integral_constant<int, 2 * kRedsQuarter>;
+    using Q3 = std::integral_constant<int, 3 * kRedsQuarter>;
+
+    // dQ(it): TMEM -> registers, then the TMEM columns are released.
     auto drain_dq = [&](int it) -> bool {
       if (!warp_wait(bar(DQ_FULL), it & 1, W)) return false;
       ptx::tc_fence_after();
-      constexpr int kCols = HD / 2;        // this warp's dQ columns [G * kCols, +kCols)
-      constexpr int kUnits = kCols / 16;   // 2 KB units, contiguous in the accumulator
-      uint32_t r[kCols];
       if constexpr (kCols == 64) {
         ptx::tmem_ld64(tm + Ly::kColdQ + lane_off + G * 64, tm + Ly::kColdQ + lane_off + G * 64 + 32,
-                       *reinterpret_cast<uint32_t(*)[64]>(r));
+                       *reinterpret_cast<uint32_t(*)[64]>(dq));
       } else {
-        ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(r));
+        ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(dq));
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DQ_EMPTY));
-      float* unit0 = prm.dq_accum + dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * kUnits, HD);
-      if (qq == 1) {
+      dq_dst = prm.dq_accum + dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * kUnits, HD);
+      if (staged) {
         const uint32_t buf = sbase + Ly::kStage + G * (2 * kUnits * 2048) + (rounds & 1) * (kUnits * 2048);
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         __syncwarp();
@@ -414,21 +448,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < kUnits; ++u)
 #pragma unroll
           for (int g = 0; g < 4; ++g)
-            ptx::st_shared_v4(buf + u * 2048 + g * 512 + lane * 16, r[u * 16 + 4 * g], r[u * 16 + 4 * g + 1],
-                              r[u * 16 + 4 * g + 2], r[u * 16 + 4 * g + 3]);
+            ptx::st_shared_v4(buf + u * 2048 + g * 512 + lane * 16, dq[u * 16 + 4 * g], dq[u * 16 + 4 * g + 1],
+                              dq[u * 16 + 4 * g + 2], dq[u * 16 + 4 * g + 3]);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::bulk_reduce_add_f32(unit0, buf, kUnits * 2048);
+          ptx::bulk_reduce_add_f32(dq_dst, buf, kUnits * 2048);
           ptx::bulk_commit();
         }
         ++rounds;
+      } else if (kSplitReds) {
+        pending = true;
       } else {
-#pragma unroll
-        for (int m = 0; m < kCols / 4; ++m)
-          ptx::red_add_v4(unit0 + (m / 4) * kDqUnitFloats + (m % 4) * 128 + lane * 4, __uint_as_float(r[4 * m]),
-                          __uint_as_float(r[4 * m + 1]), __uint_as_float(r[4 * m + 2]),
-                          __uint_as_float(r[4 * m + 3]));
+        issue_reds(Q0{});
+        issue_reds(Q1{});
+        issue_reds(Q2{});
+        issue_reds(Q3{});
       }
       return true;
     };
@@ -438,32 +473,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = i & 1;
       const uint32_t ph = i & 1;
       const int q0 = (q_first + i) * kBlk;
-      // ---- P(i)
+      // ---- P(i); the second half of the pending reductions goes between its halves
       if (!(ok = warp_wait(bar(S_FULL), ph, W))) break;
       if (!(ok = warp_wait(bar(QFULL0 + st), (i >> 1) & 1, W))) break;
       ptx::tc_fence_after();
       {
-        uint32_t r[64];
-        ptx::tmem_ld64(tm + Ly::kColS + lane_off + c0, tm + Ly::kColS + lane_off + c0 + 32, r);
         const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4 + c0 * 4;
         const bool diag = prm.causal && q0 == k0;
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-          const float4 l4 = ptx::ld_shared_f4(sLa + j * 4);
-          float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
-          float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
-          float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
-          float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
-          if (diag) {  // key k0 + t is visible to query q0 + col iff t <= col
-            const int col = c0 + j;
-            p0 = col + 0 < t ? 0.f : p0;
-            p1 = col + 1 < t ? 0.f : p1;
-            p2 = col + 2 < t ? 0.f : p2;
-            p3 = col + 3 < t ? 0.f : p3;
+        for (int hf = 0; hf < kHalves; ++hf) {
+          uint32_t r[kW];
+          tmem_ld_cols(tm + Ly::kColS + lane_off + c0 + kW * hf, r);
+#pragma unroll
+          for (int j = 0; j < kW; j += 4) {
+            const float4 l4 = ptx::ld_shared_f4(sLa + (kW * hf + j) * 4);
+            float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
+            float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
+            float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
+            float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
+            if (diag) {  // key k0 + t is visible to query q0 + col iff t <= col
+              const int col = c0 + kW * hf + j;
+              p0 = col + 0 < t ? 0.f : p0;
+              p1 = col + 1 < t ? 0.f : p1;
+              p2 = col + 2 < t ? 0.f : p2;
+              p3 = col + 3 < t ? 0.f : p3;
+            }
+            pk[kW / 2 * hf + j / 2] = ptx::pack_bf16x2(p0, p1);
+            pk[kW / 2 * hf + j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
           }
-          pk[j / 2] = ptx::pack_bf16x2(p0, p1);
-          pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+          if (kSplitReds && pending) {
+            if (hf == 0) issue_reds(Q2{});
+            else issue_reds(Q3{});
+          }
         }
+        if (kSplitReds) pending = false;
         if (!key_ok) {
 #pragma unroll
           for (int k = 0; k < 32; ++k) pk[k] = 0u;
@@ -476,39 +519,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_arrive(bar(P_FULL));
       // ---- dQ(i-1); also guarantees dS(i-1) has been consumed
       if (i > 0 && !(ok = drain_dq(i - 1))) break;
-      // ---- dS(i)
+      // ---- dS(i); the first half of dQ(i-1)'s reductions goes between its halves
       if (!(ok = warp_wait(bar(DP_FULL), ph, W))) break;
       ptx::tc_fence_after();
       {
-        uint32_t r[64];
-        ptx::tmem_ld64(tm + Ly::kColdP + lane_off + c0, tm + Ly::kColdP + lane_off + c0 + 32, r);
         const uint32_t sDa = sbase + Ly::kD + st * kBlk * 4 + c0 * 4;
-        uint32_t ds[32];
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-          const float4 d4 = ptx::ld_shared_f4(sDa + j * 4);
-          const uint32_t pa = pk[j / 2], pb = pk[j / 2 + 1];
-          const float ds0 = ptx::bf16lo(pa) * (__uint_as_float(r[j + 0]) - d4.x);
-          const float ds1 = ptx::bf16hi(pa) * (__uint_as_float(r[j + 1]) - d4.y);
-          const float ds2 = ptx::bf16lo(pb) * (__uint_as_float(r[j + 2]) - d4.z);
-          const float ds3 = ptx::bf16hi(pb) * (__uint_as_float(r[j + 3]) - d4.w);
-          ds[j / 2] = ptx::pack_bf16x2(ds0, ds1);
-          ds[j / 2 + 1] = ptx::pack_bf16x2(ds2, ds3);
-        }
         // row t of dS^T, query columns [c0, c0 + 64) = chunk G: eight 16-byte
         // pieces, 128-byte swizzle (piece index XOR row % 8)
         const uint32_t row = sdS + G * Ly::kChunk + t * 128;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          ptx::st_shared_v4(row + (((uint32_t)u ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1],
-                            ds[4 * u + 2], ds[4 * u + 3]);
+        for (int hf = 0; hf < kHalves; ++hf) {
+          uint32_t r[kW];
+          tmem_ld_cols(tm + Ly::kColdP + lane_off + c0 + kW * hf, r);
+          uint32_t ds[kW / 2];
+#pragma unroll
+          for (int j = 0; j < kW; j += 4) {
+            const float4 d4 = ptx::ld_shared_f4(sDa + (kW * hf + j) * 4);
+            const uint32_t pa = pk[kW / 2 * hf + j / 2], pb = pk[kW / 2 * hf + j / 2 + 1];
+            const float ds0 = ptx::bf16lo(pa) * (__uint_as_float(r[j + 0]) - d4.x);
+            const float ds1 = ptx::bf16hi(pa) * (__uint_as_float(r[j + 1]) - d4.y);
+            const float ds2 = ptx::bf16lo(pb) * (__uint_as_float(r[j + 2]) - d4.z);
+            const float ds3 = ptx::bf16hi(pb) * (__uint_as_float(r[j + 3]) - d4.w);
+            ds[j / 2] = ptx::pack_bf16x2(ds0, ds1);
+            ds[j / 2 + 1] = ptx::pack_bf16x2(ds2, ds3);
+          }
+#pragma unroll
+          for (int u = 0; u < kW / 8; ++u) {
+            const uint32_t piece = (uint32_t)(kW / 8 * hf + u);
+            ptx::st_shared_v4(row + ((piece ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1], ds[4 * u + 2],
+                              ds[4 * u + 3]);
+          }
+          if (pending) {
+            if (hf == 0) issue_reds(Q0{});
+            else issue_reds(Q1{});
+          }
+        }
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DS_FULL));
     }
+    if (ok && pending) {  // second half of dQ(n-2)
+      issue_reds(Q2{});
+      issue_reds(Q3{});
+      pending = false;
+    }
     if (ok && n_iter > 0) ok = drain_dq(n_iter - 1);
-    if (lane == 0) ptx::bulk_wait_all();  // this warp's reductions are complete
+    if (ok && pending) {
+      issue_reds(Q0{});
+      issue_reds(Q1{});
+      issue_reds(Q2{});
+      issue_reds(Q3{});
+    }
+    if (lane == 0) ptx::bulk_wait_all();  // this warp's bulk reductions are complete
     __syncwarp();
     if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
       ptx::tc_fence_after();
