@@ -299,7 +299,11 @@ fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* 
   fa_status st = validate(p);
   if (st != FA_OK) return st;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(L)) return FA_ERR_INVALID_ARG;
-  return from_cuda(fa::launch_fwd_simt(*p, Q, K, V, O, L, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  if (p->dtype == FA_FP32) return from_cuda(fa::launch_fwd_simt(*p, Q, K, V, O, L, s));
+  int32_t* status = fa::device_status_word();
+  if (!status) return FA_ERR_CUDA;
+  return from_cuda(fa::launch_fwd_sm103(*p, Q, K, V, O, L, status, fa::wait_limit_ns(), s));
 }
 
 fa_status fa_bwd_preprocess(const fa_problem* p, const void* O, const void* dO, float* D, float* dQ_accum,

@@ -590,7 +590,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------- host side
+template <int HD>
+cudaError_t launch_hd(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t s) {
+  using Ly = Layout<HD>;
+  cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
+  bwd_sm103_kernel<HD><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -604,10 +616,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   });
   return fn;
 }
+}  // namespace
 
 // [B, H, N, d] bf16 tensor as a 4-D TMA map with 64 x 128 boxes, 128-byte
 // swizzle; rows past N read as zeros.
-bool make_map(CUtensorMap* m, const void* base, const fa_problem& p) {
+bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)p.H, (cuuint64_t)p.B};
@@ -620,24 +633,12 @@ bool make_map(CUtensorMap* m, const void* base, const fa_problem& p) {
   return r == CUDA_SUCCESS;
 }
 
-template <int HD>
-cudaError_t launch_hd(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t s) {
-  using Ly = Layout<HD>;
-  cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
-  bwd_sm103_kernel<HD><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
 cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
                              const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
                              uint64_t wait_ns, cudaStream_t s) {
   CUtensorMap maps[4];
-  if (!make_map(&maps[0], Q, p) || !make_map(&maps[1], K, p) || !make_map(&maps[2], V, p) ||
-      !make_map(&maps[3], dO, p))
+  if (!make_bf16_tile_map(&maps[0], Q, p) || !make_bf16_tile_map(&maps[1], K, p) ||
+      !make_bf16_tile_map(&maps[2], V, p) || !make_bf16_tile_map(&maps[3], dO, p))
     return cudaErrorInvalidValue;
   BwdParams prm;
   prm.L = L;

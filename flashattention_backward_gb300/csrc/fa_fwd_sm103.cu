@@ -1,0 +1,401 @@
+// Forward pass (companion of the backward) for bf16, head dim 64 or 128, on
+// the sm_100-family tensor cores.  Online softmax over 128-key blocks
+// (1point3acres FlashAttention write-up, online-softmax paragraphs; "CUDA
+// 算子工程" ch.16 §16.4 for L = m + log l):
+//   m' = max(m, rowmax(S_b)),  alpha = exp(m - m'),  l' = alpha l + sum(p_b),
+//   O' = alpha O + p_b V_b,    O = O' / l,  L = m + log l.
+//
+// One CTA owns a 128-row query block (resident in shared memory) and walks
+// the key blocks it can see (all, or up to the diagonal under the causal
+// mask).  S = Q K_b^T goes to one of two TMEM buffers (so S_{b+1} is computed
+// while S_b is turned into P_b); P_b (bf16) is written over S_b and feeds
+// O += P_b V_b straight from TMEM; O accumulates in TMEM.
+//
+// The exponent base m is only moved when a row maximum grows by more than
+// 2^8 (in exp2 units): otherwise P = exp2(S - m) <= 256 stays well inside
+// fp32 and bf16, and O, l keep the old base, so O in TMEM is rescaled only
+// on those rare steps.  The final O / l and L = m + log l are exact for any
+// base.
+//
+// Warp roles (320 threads):
+//   warps 0-7  softmax.  Warp w owns query rows 32*(w%4) .. +31 (its TMEM lane
+//              quarter) and key columns [64*(w/4), +64) of each block; the two
+//              warps of a lane quarter exchange row maxima through shared
+//              memory.  Epilogue: O columns [d/2 * (w/4), +d/2) and L.
+//   warp  8    TMA producer: Q once, K and V double-buffered.
+//   warp  9    TMEM allocator and MMA issuer (one elected lane).
+//
+// Every wait is bounded (same mechanism as the backward kernel).
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p);  // fa_bwd_sm103.cu
+
+namespace {
+
+constexpr int kBlk = 128;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+enum BarId {
+  Q_FULL = 0,
+  KV_FULL0,   // K, V stage landed
+  KV_FULL1,
+  KV_EMPTY0,  // K, V stage free again
+  KV_EMPTY1,
+  S_FULL0,    // S_b in TMEM buffer 0
+  S_FULL1,
+  P_FULL0,    // P_b in TMEM buffer 0 (256 arrivals)
+  P_FULL1,
+  O_DONE,     // O += P_b V_b done
+  DRAIN,      // every MMA done (waited only when a CTA gives up)
+  kNumBars
+};
+
+template <int HD>
+struct FwdLayout {
+  static constexpr int kChunk = kBlk * 128;
+  static constexpr int kTile = kBlk * HD * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTile;          // 2 stages
+  static constexpr int kV = kK + 2 * kTile;      // 2 stages
+  static constexpr int kX = kV + 2 * kTile;      // exchange: [2 parities (max) + 1 (sum)][2 halves][128] fp32
+  static constexpr int kBar = kX + 3 * 2 * kBlk * 4;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kBytes <= 232448, "shared memory budget");
+};
+
+struct FwdParams {
+  __nv_bfloat16* O;
+  float* L;
+  int32_t* status;
+  uint64_t wait_ns;
+  int B, H, N;
+  int n_tiles;
+  int64_t sb, sh, sn;
+  float scale;
+  int causal;
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const ptx::Waiter& w) {
+  return __all_sync(0xffffffffu, ptx::wait_bounded(bar, parity, w, true));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const FwdParams prm) {
+  using Ly = FwdLayout<HD>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicCAS(prm.status, 0, (int32_t)FA_ERR_DEVICE);
+    return;
+  }
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kMisc + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + Ly::kBar + 8 * i; };
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(Q_FULL), 1);
+    ptx::mbar_init(bar(KV_FULL0), 1);
+    ptx::mbar_init(bar(KV_FULL1), 1);
+    ptx::mbar_init(bar(KV_EMPTY0), 1);
+    ptx::mbar_init(bar(KV_EMPTY1), 1);
+    ptx::mbar_init(bar(S_FULL0), 1);
+    ptx::mbar_init(bar(S_FULL1), 1);
+    ptx::mbar_init(bar(P_FULL0), kSoftmaxThreads);
+    ptx::mbar_init(bar(P_FULL1), kSoftmaxThreads);
+    ptx::mbar_init(bar(O_DONE), 1);
+    ptx::mbar_init(bar(DRAIN), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(sbase + Ly::kMisc, Ly::kTmemCols);
+    ptx::tmem_relinquish();
+    ptx::tc_fence_before();
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tm = __shfl_sync(0xffffffffu, *tmem_slot, 0);
+
+  // work item: query block qt of head (b, h); heads one after another (K, V
+  // of a head shared in L2), the longest causal walk first inside a head
+  const int bh = blockIdx.x / prm.n_tiles;
+  const int qt = prm.n_tiles - 1 - blockIdx.x % prm.n_tiles;
+  const int b = bh / prm.H, h = bh % prm.H;
+  const int q0 = qt * kBlk;
+  const int n_blk = prm.causal ? qt + 1 : prm.n_tiles;
+  const int64_t head = (int64_t)b * prm.sb + (int64_t)h * prm.sh;
+  const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
+  const uint32_t sQ = sbase + Ly::kQ;
+  auto sK = [&](int st) -> uint32_t { return sbase + Ly::kK + st * Ly::kTile; };
+  auto sV = [&](int st) -> uint32_t { return sbase + Ly::kV + st * Ly::kTile; };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    int issued = 0;
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tmQ);
+      ptx::prefetch_tensormap(&tmK);
+      ptx::prefetch_tensormap(&tmV);
+      ptx::mbar_arrive_expect_tx(bar(Q_FULL), Ly::kTile);
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) ptx::tma_load_4d(sQ + c * Ly::kChunk, &tmQ, bar(Q_FULL), c * 64, q0, h, b);
+    }
+    for (int j = 0; j < n_blk; ++j) {
+      const int st = j & 1;
+      if (j >= 2 && !(ok = warp_wait(bar(KV_EMPTY0 + st), ((j - 2) >> 1) & 1, W))) break;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(KV_FULL0 + st), 2 * Ly::kTile);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c) {
+          ptx::tma_load_4d(sK(st) + c * Ly::kChunk, &tmK, bar(KV_FULL0 + st), c * 64, j * kBlk, h, b);
+          ptx::tma_load_4d(sV(st) + c * Ly::kChunk, &tmV, bar(KV_FULL0 + st), c * 64, j * kBlk, h, b);
+        }
+      }
+      __syncwarp();
+      issued = j + 1;
+    }
+    if (!ok) {
+      ptx::wait_bounded(bar(Q_FULL), 0, W, false);
+      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
+        ptx::wait_bounded(bar(KV_FULL0 + (j & 1)), (j >> 1) & 1, W, false);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issue
+    constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
+    constexpr uint32_t kIdO = ptx::idesc_bf16_f32(128, HD, false, true);    // O += P V
+    auto kdesc = [&](uint32_t tile, int kk) -> uint64_t {
+      return ptx::sdesc_sw128(tile + (kk >> 2) * Ly::kChunk + (kk & 3) * 32, 16, 1024);
+    };
+    auto mndesc = [&](uint32_t tile, int kk) -> uint64_t {
+      return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
+    };
+    const uint32_t tO = tm + Ly::kColO;
+    auto issue_S = [&](int j) {
+      const uint32_t tS = tm + ((j & 1) ? Ly::kColS1 : Ly::kColS0);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS, kdesc(sQ, kk), kdesc(sK(j & 1), kk), kIdS, kk > 0);
+      ptx::tc_commit(bar(S_FULL0 + (j & 1)));
+    };
+    bool ok = warp_wait(bar(Q_FULL), 0, W) && warp_wait(bar(KV_FULL0), 0, W);
+    if (ok) {
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) issue_S(0);
+      __syncwarp();
+    }
+    if (ok && n_blk > 1) {
+      ok = warp_wait(bar(KV_FULL1), 0, W);
+      if (ok) {
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) issue_S(1);
+        __syncwarp();
+      }
+    }
+    for (int j = 0; ok && j < n_blk; ++j) {
+      const int st = j & 1;
+      // O += P_j V_j  (A = P_j from TMEM: key steps 0-3 in columns [0,32), 4-7 in [64,96))
+      if (!(ok = warp_wait(bar(P_FULL0 + st), (j >> 1) & 1, W))) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        const uint32_t tP = tm + (st ? Ly::kColS1 : Ly::kColS0);
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          ptx::mma_ts(tO, tP + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(sV(st), kk), kIdO, (j | kk) != 0);
+        ptx::tc_commit(bar(O_DONE));
+        ptx::tc_commit(bar(KV_EMPTY0 + st));
+      }
+      __syncwarp();
+      // S_{j+2} into the same TMEM buffer once P_j has been read
+      if (j + 2 < n_blk) {
+        if (!(ok = warp_wait(bar(KV_FULL0 + st), ((j + 2) >> 1) & 1, W))) break;
+        if (!(ok = warp_wait(bar(O_DONE), j & 1, W))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) issue_S(j + 2);
+        __syncwarp();
+      }
+    }
+    // the softmax warps wait for the last O_DONE; on an abort make sure no
+    // MMA is still in flight before tensor memory is freed
+    if (ptx::elect_one()) ptx::tc_commit(bar(DRAIN));
+    __syncwarp();
+    if (!ok) ptx::wait_bounded(bar(DRAIN), 0, W, false);
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int qq = warp & 3, G = warp >> 2;
+    const int t = qq * 32 + lane;          // query row in the block == TMEM lane
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    const int qrow = q0 + t;
+    const int c0 = G * 64;                 // key columns [c0, c0 + 64) of each block
+    const float sl2 = prm.scale * kLog2e;
+    float* xchg = reinterpret_cast<float*>(smem + Ly::kX);
+    float m_run = -INFINITY;               // exponent base (log2 units)
+    float l_part = 0.f;                    // this warp's part of the row sum
+    bool ok = true;
+    for (int j = 0; j < n_blk; ++j) {
+      const int st = j & 1;
+      const uint32_t tS = tm + (st ? Ly::kColS1 : Ly::kColS0);
+      if (!(ok = warp_wait(bar(S_FULL0 + st), (j >> 1) & 1, W))) break;
+      ptx::tc_fence_after();
+      uint32_t r[64];
+      ptx::tmem_ld64(tS + lane_off + c0, tS + lane_off + c0 + 32, r);
+      const int k0 = j * kBlk + c0;
+      const bool need_mask = (prm.causal && j == qt) || (j * kBlk + kBlk > prm.N);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float s = __uint_as_float(r[c]) * sl2;
+        if (need_mask) {
+          const int key = k0 + c;
+          if (key >= prm.N || (prm.causal && key > qrow)) s = -INFINITY;
+        }
+        r[c] = __float_as_uint(s);
+        mx = fmaxf(mx, s);
+      }
+      // row maximum over both halves of the block
+      xchg[(st * 2 + G) * kBlk + t] = mx;
+      named_bar_sync(1 + qq, 64);
+      mx = fmaxf(mx, xchg[(st * 2 + (G ^ 1)) * kBlk + t]);
+      float m_new = m_run;
+      bool rescale = false;
+      if (j == 0 || mx > m_run + kRescaleThreshold) {
+        m_new = fmaxf(m_run, mx);
+        rescale = j > 0;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O (this warp's columns) and l move to the new base: O *= 2^(m - m')
+        if (!(ok = warp_wait(bar(O_DONE), (j - 1) & 1, W))) break;
+        ptx::tc_fence_after();
+        const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.f;
+        constexpr int kOC = HD / 2;
+        uint32_t o[kOC];
+        if constexpr (kOC == 64) {
+          ptx::tmem_ld64(tm + Ly::kColO + lane_off + G * 64, tm + Ly::kColO + lane_off + G * 64 + 32,
+                         *reinterpret_cast<uint32_t(*)[64]>(o));
+        } else {
+          ptx::tmem_ld32(tm + Ly::kColO + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(o));
+        }
+#pragma unroll
+        for (int c = 0; c < kOC; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+#pragma unroll
+        for (int c = 0; c < kOC; c += 16) ptx::tmem_st16(tm + Ly::kColO + lane_off + G * kOC + c, &o[c]);
+        ptx::tmem_st_wait();
+        l_part *= alpha;
+      }
+      m_run = m_new;
+      const float mb = m_run == -INFINITY ? 0.f : m_run;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = ptx::ex2(__uint_as_float(r[c]) - mb);
+        const float p1 = ptx::ex2(__uint_as_float(r[c + 1]) - mb);
+        l_part += p0 + p1;
+        pk[c / 2] = ptx::pack_bf16x2(p0, p1);
+      }
+      ptx::tmem_st16(tS + lane_off + G * 64, &pk[0]);
+      ptx::tmem_st16(tS + lane_off + G * 64 + 16, &pk[16]);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(P_FULL0 + st));
+    }
+    // epilogue: O / l and L
+    if (ok) {
+      xchg[(4 + G) * kBlk + t] = l_part;
+      named_bar_sync(1 + qq, 64);
+      const float l = l_part + xchg[(4 + (G ^ 1)) * kBlk + t];
+      if (warp_wait(bar(O_DONE), (n_blk - 1) & 1, W)) {
+        ptx::tc_fence_after();
+        const float inv = 1.f / l;
+        constexpr int kOC = HD / 2;
+        __nv_bfloat16* orow = prm.O + head + (int64_t)qrow * prm.sn + G * kOC;
+#pragma unroll
+        for (int c = 0; c < kOC; c += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld32(tm + Ly::kColO + lane_off + G * kOC + c, o);
+          if (qrow < prm.N) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 v;
+              v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+              v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+              v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+              v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + c + 8 * u) = v;
+            }
+          }
+        }
+        if (G == 0 && qrow < prm.N) prm.L[(int64_t)bh * prm.N + qrow] = (m_run + log2f(l)) * kLn2;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tm, Ly::kTmemCols);
+  }
+}
+
+template <int HD>
+cudaError_t launch_fwd_hd(const fa_problem& p, const CUtensorMap* maps, const FwdParams& prm, cudaStream_t s) {
+  using Ly = FwdLayout<HD>;
+  cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
+  fwd_sm103_kernel<HD><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
+                             int32_t* status, uint64_t wait_ns, cudaStream_t s) {
+  CUtensorMap maps[3];
+  if (!make_bf16_tile_map(&maps[0], Q, p) || !make_bf16_tile_map(&maps[1], K, p) ||
+      !make_bf16_tile_map(&maps[2], V, p))
+    return cudaErrorInvalidValue;
+  FwdParams prm;
+  prm.O = (__nv_bfloat16*)O;
+  prm.L = L;
+  prm.status = status;
+  prm.wait_ns = wait_ns;
+  prm.B = p.B;
+  prm.H = p.H;
+  prm.N = p.N;
+  prm.n_tiles = (int)ceil_div(p.N, kBlk);
+  prm.sb = p.stride_b;
+  prm.sh = p.stride_h;
+  prm.sn = p.stride_n;
+  prm.scale = p.scale;
+  prm.causal = p.causal;
+  if (p.d == 64) return launch_fwd_hd<64>(p, maps, prm, s);
+  if (p.d == 128) return launch_fwd_hd<128>(p, maps, prm, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -30,6 +30,7 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO, float* D,
                               float* dq_accum, cudaStream_t s);
 cudaError_t launch_convert_dq(const fa_problem& p, const float* dq_accum, void* dQ, cudaStream_t s);
+// CUDA-core forward for float32.
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
                             void* O, float* L, cudaStream_t s);
 cudaError_t launch_bwd_simt_fp32(const fa_problem& p, const float* Q, const float* K, const float* V,
@@ -40,6 +41,9 @@ cudaError_t launch_bwd_simt_fp32(const fa_problem& p, const float* Q, const floa
 cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V,
                              const void* dO, const float* L, const float* D, float* dq_accum,
                              void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
+// tcgen05 forward for bf16, d in {64, 128}.
+cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
+                             int32_t* status, uint64_t wait_ns, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t wait_ns, cudaStream_t s);
 
 }  // namespace fa

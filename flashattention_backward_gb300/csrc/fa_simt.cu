@@ -1,8 +1,8 @@
-// CUDA-core (FFMA) kernels:
-//  * the forward pass for both storage types (fp32 math, online softmax);
-//  * the exact-fp32 backward used when Q, K, V, dO are float32 (tensor cores
-//    have no fp32 mode that keeps float32 accuracy, and the fp32 workload is
-//    a small correctness problem).
+// CUDA-core (FFMA) kernels for float32 problems (tensor cores have no fp32
+// mode that keeps float32 accuracy, and the fp32 workload is a small
+// correctness problem):
+//  * the forward pass (online softmax);
+//  * the backward pass.
 // Both use 64 x 64 tiles and 256 threads arranged 16 x 16; thread (ty, tx)
 // owns rows ty + 16a and columns tx + 16b of a tile, so the lanes that share
 // a row sit in one half-warp and reduce with 4 shuffles.
@@ -25,9 +25,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void from_f(float* p, float v) { *p = v; }
-__device__ __forceinline__ void from_f(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // Copy a kT x HD tile of rows [row0, row0 + kT) into shared memory as fp32
 // with row pitch `pitch`; rows >= N are zero.
@@ -373,7 +371,6 @@ cudaError_t launch_bwd_fp32_t(const fa_problem& p, const float* Q, const float* 
 
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                             cudaStream_t s) {
-  if (p.dtype == FA_BF16) return launch_fwd_dt<__nv_bfloat16>(p, Q, K, V, O, L, s);
   return launch_fwd_dt<float>(p, Q, K, V, O, L, s);
 }
 

@@ -80,6 +80,26 @@ def test_forward_four_numbers_across_a_tile_boundary():
     assert abs(L[0, 0, 0].item() - (10 + np.log(64 + 64 * np.exp(-10.0)))) < 1e-5
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_forward_four_numbers_new_max_in_later_block(d):
+    """Same example on the tensor-core forward: 128 keys of score 0, then
+    128 keys of score 10.  The second key block raises the row maximum by
+    14.4 in exp2 units, so the running base moves and O is rescaled."""
+    N = 256
+    q = torch.zeros(1, 1, N, d)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, 1, N, d)
+    k[0, 0, 128:, 0] = 10.0
+    v = torch.zeros(1, 1, N, d)
+    v[0, 0, 128:, :] = 1.0
+    to = lambda t: t.to(torch.bfloat16).to(DEV)
+    o, L = fa.attention_forward(to(q), to(k), to(v), 1.0, False)
+    torch.cuda.synchronize()
+    assert fa.get_device_status() == 0
+    assert abs(o[0, 0, 0, 0].float().item() - 0.9999546) < 4e-3  # bf16 output, not the naive 0.5
+    assert abs(L[0, 0, 0].item() - (10 + np.log(128 + 128 * np.exp(-10.0)))) < 1e-4
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp32_tiny_workload(causal):
     w = workload("tiny", causal=causal)
