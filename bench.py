@@ -213,6 +213,7 @@ def main(argv=None) -> int:
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--e2e-group", type=int, default=0, help="heads per group in the end-to-end leg (0: auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true", help="bitwise reproducible dQ (per-key-block slices)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 
@@ -242,7 +243,7 @@ def main(argv=None) -> int:
     q_h, k_h, v_h, g_h = make_inputs(w)
     q, k, v, g = (t.to(dev) for t in (q_h, k_h, v_h, g_h))
     stream = torch.cuda.current_stream()
-    p = fa.problem_for(q, w.scale, w.causal)
+    p = fa.problem_for(q, w.scale, w.causal, args.deterministic)
     o = torch.empty_like(q)
     L = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
     D = torch.empty_like(L)
@@ -321,7 +322,7 @@ def main(argv=None) -> int:
 
         def e2e_step():
             fa.attention_backward_host(hq, hk, hv, ho, hg, hL, w.scale, w.causal, args.e2e_group, workspace=ws,
-                                       out=houts, stream=stream)
+                                       out=houts, stream=stream, deterministic=args.deterministic)
 
         for _ in range(3):
             e2e_step()
@@ -346,13 +347,17 @@ def main(argv=None) -> int:
     value = whole_job_tflops(flops, world, args.steps, total_ms)
     bwd_tflops = flops / (bwd_ms * 1e-3) / 1e12
     bhnd = w.B * w.H * w.N * w.d
-    pre_bytes = 2 * bhnd * 2 + w.B * w.H * w.N * 4 + fa.fa_dq_accum_elems(p) * 4
-    cvt_bytes = fa.fa_dq_accum_elems(p) * 4 + bhnd * 2
+    slice_bytes = fa.fa_dq_accum_elems(fa.problem_for(q, w.scale, w.causal)) * 4  # one accumulator slice
+    n_slices = fa.fa_dq_accum_elems(p) * 4 // slice_bytes
+    pre_bytes = 2 * bhnd * 2 + w.B * w.H * w.N * 4 + (0 if args.deterministic else slice_bytes)
+    # convert reads every slice that holds a contribution (half of them under the causal mask)
+    live = n_slices if not w.causal else (n_slices + 1) / 2
+    cvt_bytes = slice_bytes * live + bhnd * 2
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(w, world),
+        "config": dict(workload_config(w, world), dq_mode="deterministic" if args.deterministic else "atomic"),
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "roofline": {"kernel": "fa_bwd (bwd_sm103_kernel)", "bound": "tensor", "achieved": bwd_tflops,

@@ -25,6 +25,7 @@ from . import _build
 __all__ = [
     "FaError",
     "FaProblem",
+    "FA_FLAG_DETERMINISTIC",
     "problem_for",
     "fa_dq_accum_elems",
     "fa_fwd",
@@ -46,6 +47,7 @@ __all__ = [
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_DEVICE = range(6)
 FA_BF16, FA_FP32 = 0, 1
+FA_FLAG_DETERMINISTIC = 1
 TILE_ROWS = 128
 
 
@@ -64,7 +66,7 @@ class FaProblem(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("causal", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
         ("stride_b", ctypes.c_int64),
         ("stride_h", ctypes.c_int64),
         ("stride_n", ctypes.c_int64),
@@ -136,14 +138,15 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def problem_for(q: torch.Tensor, scale: float, causal: bool) -> FaProblem:
+def problem_for(q: torch.Tensor, scale: float, causal: bool, deterministic: bool = False) -> FaProblem:
     """Problem descriptor for [B, H, N, d] tensors laid out like ``q``."""
     if q.dim() != 4:
         raise ValueError("expected a [B, H, N, d] tensor")
     if q.stride(3) != 1:
         raise ValueError("the last dimension must be contiguous")
     B, H, N, d = q.shape
-    return FaProblem(B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), 0,
+    flags = FA_FLAG_DETERMINISTIC if deterministic else 0
+    return FaProblem(B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), flags,
                      q.stride(0), q.stride(1), q.stride(2))
 
 
@@ -230,9 +233,10 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
     return o, L
 
 
-def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, stream=None, workspace=None):
+def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, stream=None, workspace=None,
+                       deterministic: bool = False):
     """dQ, dK, dV.  ``workspace`` may pass preallocated (D, dq_accum)."""
-    p = problem_for(q, scale, causal)
+    p = problem_for(q, scale, causal, deterministic)
     if workspace is None:
         D = torch.empty((p.B, p.H, p.N), dtype=torch.float32, device=q.device)
         acc = torch.empty(fa_dq_accum_elems(p), dtype=torch.float32, device=q.device)
@@ -265,9 +269,9 @@ def fa_backward_host(p: FaProblem, q, k, v, o, do, L, dq, dk, dv, workspace, hea
 
 
 def attention_backward_host(q, k, v, o, do, L, scale: float, causal: bool = False, heads_per_group: int = 0,
-                            workspace=None, out=None, stream=None):
+                            workspace=None, out=None, stream=None, deterministic: bool = False):
     """dQ, dK, dV (pinned host tensors) for host-resident inputs."""
-    p = problem_for(q, scale, causal)
+    p = problem_for(q, scale, causal, deterministic)
     if workspace is None:
         workspace = torch.empty(fa_backward_host_workspace_bytes(p, heads_per_group), dtype=torch.uint8,
                                 device="cuda")

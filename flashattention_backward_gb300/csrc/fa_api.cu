@@ -78,7 +78,8 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                                                          float* __restrict__ D, float* __restrict__ dq_accum,
                                                          int H, int N, int64_t sb, int64_t sh, int64_t sn,
-                                                         int tiles_per_head) {
+                                                         int tiles_per_head, int zero_slices,
+                                                         int64_t slice_elems) {
   constexpr int kVec = Vec16<T>::kElems;
   constexpr int kLanesPerRow = HD / kVec;          // 4 .. 32, a power of two
   constexpr int kRowsPerStep = 256 / kLanesPerRow;
@@ -109,11 +110,14 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ O
     const int n = tile * kTileRows + s * kRowsPerStep + row_in_step;
     if (sub == 0 && n < N) D[(int64_t)bh * N + n] = acc[s];
   }
-  // zero this tile of the accumulator: 128 * HD floats
-  float4* z = reinterpret_cast<float4*>(dq_accum + ((int64_t)bh * tiles_per_head + tile) * (int64_t)kTileRows * HD);
+  // zero this tile of the accumulator (128 * HD floats) in each slice
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < zero_slices; ++s) {
+    float4* z = reinterpret_cast<float4*>(dq_accum + s * slice_elems +
+                                          ((int64_t)bh * tiles_per_head + tile) * (int64_t)kTileRows * HD);
 #pragma unroll 4
-  for (int k = threadIdx.x; k < kTileRows * HD / 4; k += 256) z[k] = zero;
+    for (int k = threadIdx.x; k < kTileRows * HD / 4; k += 256) z[k] = zero;
+  }
 }
 
 template <typename T>
@@ -121,10 +125,15 @@ static cudaError_t launch_preprocess_t(const fa_problem& p, const T* O, const T*
                                        cudaStream_t s) {
   const int tiles = (int)ceil_div(p.N, kTileRows);
   const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
+  // Deterministic bf16: every slice element the convert reads is written by
+  // the backward kernel, so nothing needs zeroing.  Deterministic fp32: the
+  // 64-row kernel leaves parts of some slices untouched; zero them all.
+  const int zero_slices = !deterministic(p) ? 1 : (p.dtype == FA_BF16 ? 0 : (int)dq_slices(p));
+  const int64_t slice_elems = dq_slice_elems(p);
 #define FA_PRE_CASE(HDV)                                                                                    \
   case HDV:                                                                                                 \
     preprocess_kernel<T, HDV><<<grid, 256, 0, s>>>(O, dO, D, acc, p.H, p.N, p.stride_b, p.stride_h,        \
-                                                   p.stride_n, tiles);                                      \
+                                                   p.stride_n, tiles, zero_slices, slice_elems);            \
     break;
   switch (p.d) {
     FA_PRE_CASE(16)
@@ -165,10 +174,11 @@ __device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float* v, in
   }
 }
 
-template <typename T, int HD>
+template <typename T, int HD, bool kSlices>
 __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict__ acc, T* __restrict__ dQ, int H,
                                                          int N, int64_t sb, int64_t sh, int64_t sn,
-                                                         int tiles_per_head, float scale) {
+                                                         int tiles_per_head, float scale, int slices,
+                                                         int64_t slice_elems, int causal, int kb_rows) {
   constexpr int kPitch = HD + 4;  // floats; keeps 16-byte alignment, staggers banks
   extern __shared__ float4 smem_f4[];
   float* tile_s = reinterpret_cast<float*>(smem_f4);
@@ -176,12 +186,28 @@ __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict
   const int bh = blockIdx.x / tiles_per_head;
   const int b = bh / H, h = bh % H;
   const float4* src = reinterpret_cast<const float4*>(acc + dq_unit_offset(bh, tiles_per_head, tile, 0, 0, HD));
+  // Key blocks that touch this query tile: all, or (causal) those starting at
+  // or before its last row.  Their slices are summed in increasing order.
+  int last = slices - 1;
+  if (causal && slices > 1) {
+    const int lim = (tile * kTileRows + kTileRows - 1) / kb_rows;
+    last = lim < last ? lim : last;
+  }
+  const int64_t slice4 = slice_elems / 4;
   // a tile is 4 x (HD/16) units of [4 column groups][32 rows][4 columns]
 #pragma unroll 4
   for (int k = threadIdx.x; k < kTileRows * HD / 4; k += 256) {
     const int unit = k / 128, g = (k % 128) / 32, r = k % 32;
     const int row = (unit / (HD / 16)) * 32 + r, col = (unit % (HD / 16)) * 16 + g * 4;
-    const float4 v = __ldg(src + k);
+    float4 v = __ldg(src + k);
+    if (kSlices)
+      for (int sl = 1; sl <= last; ++sl) {
+        const float4 w = __ldg(src + sl * slice4 + k);
+        v.x += w.x;
+        v.y += w.y;
+        v.z += w.z;
+        v.w += w.w;
+      }
     *reinterpret_cast<float4*>(tile_s + row * kPitch + col) = v;
   }
   __syncthreads();
@@ -205,13 +231,13 @@ static cudaError_t launch_convert_t(const fa_problem& p, const float* acc, T* dQ
 #define FA_CONV_CASE(HDV)                                                                                  \
   case HDV: {                                                                                              \
     const size_t sm = (size_t)kTileRows * (HDV + 4) * sizeof(float);                                      \
+    auto kern = deterministic(p) ? convert_dq_kernel<T, HDV, true> : convert_dq_kernel<T, HDV, false>;    \
     if (sm > 48 * 1024) {                                                                                  \
-      cudaError_t e = cudaFuncSetAttribute(convert_dq_kernel<T, HDV>,                                      \
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);          \
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);    \
       if (e != cudaSuccess) return e;                                                                      \
     }                                                                                                      \
-    convert_dq_kernel<T, HDV><<<grid, 256, sm, s>>>(acc, dQ, p.H, p.N, p.stride_b, p.stride_h, p.stride_n, \
-                                                    tiles, p.scale);                                       \
+    kern<<<grid, 256, sm, s>>>(acc, dQ, p.H, p.N, p.stride_b, p.stride_h, p.stride_n, tiles, p.scale,      \
+                               (int)dq_slices(p), dq_slice_elems(p), p.causal, key_block_rows(p));         \
     break;                                                                                                 \
   }
   switch (p.d) {
@@ -267,7 +293,7 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 fa_status validate(const fa_problem* p) {
   if (!p) return FA_ERR_INVALID_ARG;
   if (p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) return FA_ERR_INVALID_ARG;
-  if (p->reserved != 0) return FA_ERR_INVALID_ARG;
+  if (p->flags & ~(int32_t)FA_FLAG_DETERMINISTIC) return FA_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return FA_ERR_INVALID_ARG;
   if (!(p->scale == p->scale) || p->scale <= 0.f || p->scale > 1e30f) return FA_ERR_INVALID_ARG;
   if (p->dtype != FA_BF16 && p->dtype != FA_FP32) return FA_ERR_INVALID_ARG;
@@ -291,7 +317,7 @@ extern "C" {
 
 size_t fa_dq_accum_elems(const fa_problem* p) {
   if (validate(p) != FA_OK) return 0;
-  return (size_t)p->B * p->H * fa::ceil_div(p->N, fa::kTileRows) * fa::kTileRows * p->d;
+  return (size_t)(fa::dq_slices(*p) * fa::dq_slice_elems(*p));
 }
 
 fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* V, void* O, float* L,

@@ -121,6 +121,7 @@ struct BwdParams {
   int64_t sb, sh, sn;
   float scale;
   int causal;
+  int64_t slice_elems;  // > 0: deterministic, key block kb stores into slice kb
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const ptx::Waiter& w) {
@@ -149,7 +150,7 @@ __device__ __forceinline__ void store_row(uint32_t taddr, bool valid, __nv_bfloa
   }
 }
 
-template <int HD>
+template <int HD, bool kDet>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -414,13 +415,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* dq_dst = nullptr;               // its first unit in the accumulator
     bool pending = false;                  // reductions of dq still to issue
 
+    constexpr bool det = kDet;             // store into this key block's slice instead of adding
     auto issue_reds = [&](auto m0c) {      // reductions m0 .. m0 + kRedsQuarter - 1
       constexpr int m0 = decltype(m0c)::value;
 #pragma unroll
-      for (int m = m0; m < m0 + kRedsQuarter; ++m)
-        ptx::red_add_v4(dq_dst + (m / 4) * kDqUnitFloats + (m % 4) * 128 + lane * 4, __uint_as_float(dq[4 * m]),
-                        __uint_as_float(dq[4 * m + 1]), __uint_as_float(dq[4 * m + 2]),
-                        __uint_as_float(dq[4 * m + 3]));
+      for (int m = m0; m < m0 + kRedsQuarter; ++m) {
+        float* a = dq_dst + (m / 4) * kDqUnitFloats + (m % 4) * 128 + lane * 4;
+        if (det)
+          ptx::st_global_v4(a, __uint_as_float(dq[4 * m]), __uint_as_float(dq[4 * m + 1]),
+                            __uint_as_float(dq[4 * m + 2]), __uint_as_float(dq[4 * m + 3]));
+        else
+          ptx::red_add_v4(a, __uint_as_float(dq[4 * m]), __uint_as_float(dq[4 * m + 1]),
+                          __uint_as_float(dq[4 * m + 2]), __uint_as_float(dq[4 * m + 3]));
+      }
     };
     using Q0 = std::integral_constant<int, 0>;
     using Q1 = std::integral_constant<int, kRedsQuarter>;
@@ -439,7 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DQ_EMPTY));
-      dq_dst = prm.dq_accum + dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * kUnits, HD);
+      dq_dst = prm.dq_accum + (det ? kb * prm.slice_elems : 0) +
+               dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * kUnits, HD);
       if (staged) {
         const uint32_t buf = sbase + Ly::kStage + G * (2 * kUnits * 2048) + (rounds & 1) * (kUnits * 2048);
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -453,7 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::bulk_reduce_add_f32(dq_dst, buf, kUnits * 2048);
+          if (det)
+            ptx::bulk_store(dq_dst, buf, kUnits * 2048);
+          else
+            ptx::bulk_reduce_add_f32(dq_dst, buf, kUnits * 2048);
           ptx::bulk_commit();
         }
         ++rounds;
@@ -590,13 +601,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HD>
+template <int HD, bool kDet>
 cudaError_t launch_hd(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t s) {
   using Ly = Layout<HD>;
-  cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(bwd_sm103_kernel<HD, kDet>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
-  bwd_sm103_kernel<HD><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  bwd_sm103_kernel<HD, kDet><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError();
 }
 
@@ -657,8 +669,10 @@ cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, 
   prm.sn = p.stride_n;
   prm.scale = p.scale;
   prm.causal = p.causal;
-  if (p.d == 64) return launch_hd<64>(p, maps, prm, s);
-  if (p.d == 128) return launch_hd<128>(p, maps, prm, s);
+  prm.slice_elems = deterministic(p) ? dq_slice_elems(p) : 0;
+  const bool det = prm.slice_elems > 0;
+  if (p.d == 64) return det ? launch_hd<64, true>(p, maps, prm, s) : launch_hd<64, false>(p, maps, prm, s);
+  if (p.d == 128) return det ? launch_hd<128, true>(p, maps, prm, s) : launch_hd<128, false>(p, maps, prm, s);
   return cudaErrorInvalidValue;
 }
 

@@ -60,7 +60,7 @@ SlotLayout slot_layout(const fa_problem& p, int g) {
   const size_t es = p.dtype == FA_BF16 ? 2 : 4;
   const size_t head = (size_t)p.N * p.d * es;
   const size_t rows = (size_t)g * p.N * 4;
-  const size_t acc = (size_t)g * ceil_div(p.N, kTileRows) * kTileRows * p.d * 4;
+  const size_t acc = (size_t)g * ceil_div(p.N, kTileRows) * kTileRows * p.d * 4 * dq_slices(p);
   SlotLayout s;
   size_t off = 0;
   for (size_t* f : {&s.q, &s.k, &s.v, &s.o, &s.dO, &s.dq, &s.dk, &s.dv}) {

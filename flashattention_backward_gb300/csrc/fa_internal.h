@@ -26,6 +26,19 @@ uint64_t wait_limit_ns();
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+inline bool deterministic(const fa_problem& p) { return (p.flags & FA_FLAG_DETERMINISTIC) != 0; }
+// Key-block height of the backward kernel that serves p (tensor-core bf16
+// kernel: 128; CUDA-core fp32 kernel: 64).
+inline int key_block_rows(const fa_problem& p) { return p.dtype == FA_BF16 ? 128 : 64; }
+// dQ accumulator slices: one per key block in deterministic mode, else one.
+inline int64_t dq_slices(const fa_problem& p) {
+  return deterministic(p) ? ceil_div(p.N, key_block_rows(p)) : 1;
+}
+// Floats in one slice: B * H * ceil(N/128) * 128 * d.
+inline int64_t dq_slice_elems(const fa_problem& p) {
+  return (int64_t)p.B * p.H * ceil_div(p.N, 128) * 128 * p.d;
+}
+
 // ---- launchers (return a cudaError_t from the launch) -------------------
 cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO, float* D,
                               float* dq_accum, cudaStream_t s);

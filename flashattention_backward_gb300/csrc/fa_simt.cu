@@ -175,7 +175,9 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_fp32_kernel(
     const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
     const float* __restrict__ dO, const float* __restrict__ Lg, const float* __restrict__ Dg,
     float* __restrict__ dq_accum, float* __restrict__ dK, float* __restrict__ dV, int H, int N, int64_t sb,
-    int64_t sh, int64_t sn, float scale, int causal) {
+    int64_t sh, int64_t sn, float scale, int causal, int64_t slice_elems) {
+  // slice_elems > 0 (deterministic): this key block's dQ contributions are
+  // stored into its own slice of the accumulator instead of added.
   constexpr int kP = HD + 1, kPP = kT + 1;
   constexpr int kCols = HD / 16;
   extern __shared__ float smem[];
@@ -303,7 +305,10 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_fp32_kernel(
 #pragma unroll
       for (int u = 0; u < kCols; ++u) {
         const int c = tx + 16 * u;
-        atomicAdd(dq_accum + dq_accum_index(bh, acc_tiles, i, c, HD), dq[a][u]);
+        if (slice_elems > 0)
+          dq_accum[kb * slice_elems + dq_accum_index(bh, acc_tiles, i, c, HD)] = dq[a][u];
+        else
+          atomicAdd(dq_accum + dq_accum_index(bh, acc_tiles, i, c, HD), dq[a][u]);
       }
     }
   }
@@ -363,7 +368,8 @@ cudaError_t launch_bwd_fp32_t(const fa_problem& p, const float* Q, const float* 
   const int tiles = (p.N + kT - 1) / kT;
   const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
   bwd_simt_fp32_kernel<HD><<<grid, kThreads, sm, s>>>(Q, K, V, dO, L, D, acc, dK, dV, p.H, p.N, p.stride_b,
-                                                      p.stride_h, p.stride_n, p.scale, p.causal);
+                                                      p.stride_h, p.stride_n, p.scale, p.causal,
+                                                      deterministic(p) ? dq_slice_elems(p) : 0);
   return cudaGetLastError();
 }
 

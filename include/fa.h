@@ -58,7 +58,9 @@
  *
  * with T = ceil(N/128).  One unit is what the tensor-core kernel stages in
  * shared memory and adds into the accumulator with one bulk reduction.
- * Padding rows receive only zero contributions.
+ * Padding rows receive only zero contributions.  With FA_FLAG_DETERMINISTIC
+ * the accumulator is a sequence of such arrays (slices), one per key block,
+ * slice k at float offset k * B*H*T*128*d.
  */
 #ifndef FA_H_
 #define FA_H_
@@ -81,17 +83,29 @@ typedef enum {
 
 typedef enum { FA_BF16 = 0, FA_FP32 = 1 } fa_dtype;
 
+/* fa_problem.flags bits. */
+typedef enum {
+  /* Bitwise reproducible dQ (ch.16 §16.3 and §16.8 item 4: extra memory buys
+   * a fixed summation order).  The accumulator then holds one slice per key
+   * block; the backward writes each key block's dQ contribution into its own
+   * slice instead of adding it, and fa_convert_dq sums the slices in
+   * increasing key-block order. */
+  FA_FLAG_DETERMINISTIC = 1
+} fa_flags;
+
 typedef struct {
   int32_t B, H, N, d;
   float scale;      /* softmax scale, normally 1/sqrt(d) */
   int32_t causal;   /* 1: key j visible to query i iff j <= i (top-left) */
   int32_t dtype;    /* fa_dtype of Q, K, V, O, dO, dQ, dK, dV */
-  int32_t reserved; /* must be 0 */
+  int32_t flags;    /* fa_flags bits (0: default mode); other bits must be 0 */
   int64_t stride_b, stride_h, stride_n; /* element strides; d is contiguous */
 } fa_problem;
 
-/* Number of float32 elements of the dQ accumulator for problem p
- * (B * H * ceil(N/128) * 128 * d), or 0 if p is NULL or invalid. */
+/* Number of float32 elements of the dQ accumulator for problem p, or 0 if p
+ * is NULL or invalid: B * H * ceil(N/128) * 128 * d, times the number of key
+ * blocks (ceil(N/128) for bf16, ceil(N/64) for fp32) with
+ * FA_FLAG_DETERMINISTIC. */
 size_t fa_dq_accum_elems(const fa_problem* p);
 
 /* Forward pass, companion of the backward: O = softmax(scale Q K^T) V and
@@ -104,7 +118,9 @@ fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* 
 
 /* Backward preprocess (ch.16 §16.8 item 1; identity of §16.1):
  * D[b,h,n] = sum_c O[b,h,n,c] * dO[b,h,n,c] in float32, and dQ_accum := 0.
- * Reads O, dO; writes D and every element of dQ_accum. */
+ * Reads O, dO; writes D and every element of dQ_accum (bf16 with
+ * FA_FLAG_DETERMINISTIC: dQ_accum is left alone, since fa_bwd overwrites
+ * every slice element fa_convert_dq reads). */
 fa_status fa_bwd_preprocess(const fa_problem* p, const void* O, const void* dO,
                             float* D, float* dQ_accum, void* stream);
 
@@ -122,7 +138,8 @@ fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* 
                  void* dK, void* dV, void* stream);
 
 /* dQ = dtype(scale * dQ_accum) (ch.16 §16.3: the convert kernel applies the
- * softmax scale and casts).  Reads dQ_accum, writes dQ. */
+ * softmax scale and casts; with FA_FLAG_DETERMINISTIC it first sums the key
+ * blocks' slices in increasing order).  Reads dQ_accum, writes dQ. */
 fa_status fa_convert_dq(const fa_problem* p, const float* dQ_accum, void* dQ, void* stream);
 
 /* The three backward calls in order: preprocess, bwd, convert. */

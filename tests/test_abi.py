@@ -41,7 +41,7 @@ def test_version_and_strings(lib):
 
 
 def _prob(**kw):
-    base = dict(B=1, H=2, N=100, d=64, scale=0.125, causal=1, dtype=fa.FA_BF16, reserved=0,
+    base = dict(B=1, H=2, N=100, d=64, scale=0.125, causal=1, dtype=fa.FA_BF16, flags=0,
                 stride_b=2 * 100 * 64, stride_h=100 * 64, stride_n=64)
     base.update(kw)
     return fa.FaProblem(**base)
@@ -53,6 +53,13 @@ def test_dq_accum_size(lib):
     p = _prob(N=48, d=16, H=1, dtype=fa.FA_FP32, stride_b=48 * 16, stride_h=48 * 16, stride_n=16)
     assert fa.fa_dq_accum_elems(p) == 128 * 16
     assert fa.fa_dq_accum_elems(_prob(d=96, stride_n=96)) == 0
+    # deterministic: one slice per key block (128 keys for bf16, 64 for fp32)
+    p = _prob(N=4000, d=128, H=16, B=4, stride_b=16 * 4000 * 128, stride_h=4000 * 128, stride_n=128,
+              flags=fa.FA_FLAG_DETERMINISTIC)
+    assert fa.fa_dq_accum_elems(p) == 32 * 4 * 16 * 32 * 128 * 128
+    p = _prob(N=48, d=16, H=1, dtype=fa.FA_FP32, stride_b=48 * 16, stride_h=48 * 16, stride_n=16,
+              flags=fa.FA_FLAG_DETERMINISTIC)
+    assert fa.fa_dq_accum_elems(p) == 1 * 128 * 16
 
 
 BAD = 0x1000  # a 16-byte aligned dummy address; validation fails before any use
@@ -67,7 +74,7 @@ BAD = 0x1000  # a 16-byte aligned dummy address; validation fails before any use
         (dict(d=32), fa.FA_ERR_UNSUPPORTED),  # bf16 path: d in {64, 128}
         (dict(causal=2), fa.FA_ERR_INVALID_ARG),
         (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
-        (dict(reserved=1), fa.FA_ERR_INVALID_ARG),
+        (dict(flags=2), fa.FA_ERR_INVALID_ARG),
         (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
         (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
         (dict(stride_n=60), fa.FA_ERR_INVALID_ARG),
