@@ -545,14 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ds[kW / 2];
 #pragma unroll
           for (int j = 0; j < kW; j += 4) {
+            // dS = P * (dP - D): the difference in fp32 (dP and D nearly
+            // cancel), then one bf16x2 product with the packed bf16 P
             const float4 d4 = ptx::ld_shared_f4(sDa + (kW * hf + j) * 4);
-            const uint32_t pa = pk[kW / 2 * hf + j / 2], pb = pk[kW / 2 * hf + j / 2 + 1];
-            const float ds0 = ptx::bf16lo(pa) * (__uint_as_float(r[j + 0]) - d4.x);
-            const float ds1 = ptx::bf16hi(pa) * (__uint_as_float(r[j + 1]) - d4.y);
-            const float ds2 = ptx::bf16lo(pb) * (__uint_as_float(r[j + 2]) - d4.z);
-            const float ds3 = ptx::bf16hi(pb) * (__uint_as_float(r[j + 3]) - d4.w);
-            ds[j / 2] = ptx::pack_bf16x2(ds0, ds1);
-            ds[j / 2 + 1] = ptx::pack_bf16x2(ds2, ds3);
+            const uint32_t g01 = ptx::pack_bf16x2(__uint_as_float(r[j + 0]) - d4.x, __uint_as_float(r[j + 1]) - d4.y);
+            const uint32_t g23 = ptx::pack_bf16x2(__uint_as_float(r[j + 2]) - d4.z, __uint_as_float(r[j + 3]) - d4.w);
+            ds[j / 2] = ptx::mul_bf16x2(pk[kW / 2 * hf + j / 2], g01);
+            ds[j / 2 + 1] = ptx::mul_bf16x2(pk[kW / 2 * hf + j / 2 + 1], g23);
           }
 #pragma unroll
           for (int u = 0; u < kW / 8; ++u) {
