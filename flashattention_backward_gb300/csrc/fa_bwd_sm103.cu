@@ -14,23 +14,25 @@
 // what dV += P^T dO and dK += dS^T Q need, and P^T feeds the dV product
 // straight from tensor memory.
 //
-// Warp roles (320 threads):
-//   warps 0-7  compute.  Warp w owns TMEM lanes 32*(w%4) .. +31 (key rows for
-//              S, dP, dV, dK; query rows for dQ) and column half w/4 of them.
+// Warp roles (576 threads):
+//   warps 0-15 compute.  Warp w owns TMEM lanes 32*(w%4) .. +31 (key rows for
+//              S, dP, dV, dK; query rows for dQ) and column quarter w/4 of
+//              them (four warps per SM sub-partition hide each other's
+//              latencies).
 //              Per query block: P = exp2(S*scale*log2e - L*log2e) -> bf16
 //              into TMEM; dQ of the previous block TMEM -> registers ->
 //              fp32 reductions into global (vector reductions, or a bulk
 //              reduction through shared memory for the warps that share an
 //              SM sub-partition with the MMA warp); dS = P * (dP - D) -> bf16
-//              into shared memory (128-byte swizzle).  Epilogue: dV (w < 4)
-//              and scale * dK (w >= 4).
-//   warp  8    TMA producer: K, V once; Q (two stages, with its L and D rows)
+//              into shared memory (128-byte swizzle).  Epilogue: dV (w < 8)
+//              and scale * dK (w >= 8), half the columns each.
+//   warp 16    TMA producer: K, V once; Q (two stages, with its L and D rows)
 //              and dO (one stage for d = 128, two for d = 64).
-//   warp  9    TMEM allocator and MMA issuer (one elected lane issues).
+//   warp 17    TMEM allocator and MMA issuer (one elected lane issues).
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
-//   [0,128)     S^T; P^T (bf16) is written over it: query columns [0,64) of
-//               S become P columns [0,32), [64,128) become [64,96)
+//   [0,128)     S^T; P^T (bf16) is written over it: query columns
+//               [32g, 32g + 32) of S become P columns [32g, 32g + 16)
 //   [128,256)   dP^T, then the dQ tile of the same step written over it
 //   [256,256+d) dV accumulator, [256+d,256+2d) dK accumulator
 //
@@ -61,8 +63,11 @@ namespace fa {
 namespace {
 
 constexpr int kBlk = 128;  // Br = Bc = 128
-constexpr int kThreads = 320;
-constexpr int kComputeThreads = 256;
+constexpr int kComputeWarps = 16;           // 4 per TMEM lane quarter
+constexpr int kProducerWarp = kComputeWarps;
+constexpr int kMmaWarp = kComputeWarps + 1;  // on the same SM sub-partition as lane quarter 1
+constexpr int kThreads = 32 * (kComputeWarps + 2);
+constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum BarId {
@@ -129,11 +134,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const p
   return __all_sync(0xffffffffu, ptx::wait_bounded(bar, parity, w, true));
 }
 
-// TMEM row (this thread's lane) of HD fp32 values -> bf16 row in global.
-template <int HD>
+// NC fp32 columns of this thread's TMEM lane -> bf16 in global.
+template <int NC>
 __device__ __forceinline__ void store_row(uint32_t taddr, bool valid, __nv_bfloat16* dst, float mul) {
 #pragma unroll
-  for (int c = 0; c < HD / 32; ++c) {
+  for (int c = 0; c < NC / 32; ++c) {
     uint32_t r[32];
     ptx::tmem_ld32(taddr + c * 32, r);
     if (valid) {
@@ -189,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(sbase + Ly::kMisc, Ly::kTmemCols);
     ptx::tmem_relinquish();
     ptx::tc_fence_before();
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sQ = [&](int st) -> uint32_t { return sbase + Ly::kQ + st * Ly::kTile; };
   auto sdO = [&](int st) -> uint32_t { return sbase + Ly::kdO + st * Ly::kTile; };
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     bool ok = true;
     int q_issued = 0, do_issued = 0;
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = do_issued > kDoSt ? do_issued - kDoSt : 0; i < do_issued; ++i)
         ptx::wait_bounded(bar(DOFULL0 + i % kDoSt), (i / kDoSt) & 1, W, false);
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     // The whole warp runs this loop and waits; one elected lane issues the
     // MMAs and commits.  Every operand is warp-uniform (the TMEM base is
@@ -325,15 +330,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = i & 1;
       const int sd = i % kDoSt;
       const uint32_t ph = i & 1;
-      // dV += P^T dO   (A = P^T from TMEM: query k-steps 0-3 in columns
-      // [0,32), 4-7 in [64,96))
+      // dV += P^T dO   (A = P^T from TMEM: the 16-query k-steps 2g, 2g+1 in
+      // columns [32g, 32g + 16))
       if (!(ok = warp_wait(bar(P_FULL), ph, W))) break;
       if (!(ok = warp_wait(bar(DOFULL0 + sd), (i / kDoSt) & 1, W))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          ptx::mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
+          ptx::mma_ts(tdV, tS + (kk >> 1) * 32 + (kk & 1) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
         ptx::tc_commit(bar(DV_DONE));
       }
       __syncwarp();
@@ -377,49 +382,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ compute
     const int qq = warp & 3;               // TMEM lane quarter
-    const int G = warp >> 2;               // column half
+    const int G = warp >> 2;               // column quarter
     const int t = qq * 32 + lane;          // TMEM lane
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
     const int kr = k0 + t;                 // key row of S, dP, dV, dK
     const bool key_ok = kr < prm.N;
     const float sl2 = prm.scale * kLog2e;
-    const int c0 = G * 64;                 // query columns [c0, c0 + 64) of S, dP
-    constexpr int kCols = HD / 2;          // this warp's dQ columns [G * kCols, +kCols)
+    const int c0 = G * 32;                 // query columns [c0, c0 + 32) of S, dP
+    constexpr int kCols = HD / 4;          // this warp's dQ columns [G * kCols, +kCols)
     constexpr int kUnits = kCols / 16;     // 2 KB units, contiguous in the accumulator
-    constexpr int kReds = kCols / 4;       // 16-byte reductions per lane per query block
-    constexpr int kRedsQuarter = kReds / 4;
-    // d = 128: half the reductions ride along with dS(i), half with P(i+1).
-    // d = 64 (half the MMA work per block, eight reductions per lane): they
-    // are issued right after the drain, which measured faster.
-    constexpr bool kSplitReds = HD == 128;
-    // S and dP columns are read from TMEM in halves where reductions ride
-    // along, else in one 64-column load.
-    constexpr int kHalves = kSplitReds ? 2 : 1;
-    constexpr int kW = 64 / kHalves;
-    auto tmem_ld_cols = [&](uint32_t taddr, uint32_t(&r)[kW]) {
-      if constexpr (kW == 64) ptx::tmem_ld64(taddr, taddr + 32, r);
-      else ptx::tmem_ld32(taddr, r);
-    };
+    constexpr int kRedsHalf = kCols / 8;   // 16-byte reductions per lane per query block, halved
     // Reductions issued on the MMA warp's SM sub-partition (lane quarter 1)
-    // delay its tcgen05.mma issue, so those two warps stage their dQ share in
+    // delay its tcgen05.mma issue, so those four warps stage their dQ share in
     // shared memory and hand it to the TMA unit as one bulk reduction (two
-    // alternating slots per warp).  The other six warps issue vector
-    // reductions from registers; at d = 128 they keep the drained dQ and
-    // issue it in quarters between the halves of the next dS and P
-    // computations, so the load/store unit sees a steady stream instead of a
-    // burst that would stall them.
+    // alternating slots per warp).  The other warps keep the drained dQ in
+    // registers and issue its vector reductions in two halves, each right
+    // after the warp has signalled its next dS and P results, so they stay
+    // off the path to those barriers.
     const bool staged = qq == 1;
-    int rounds = 0;                        // bulk reductions issued by this warp
-    uint32_t pk[32];                       // P for columns c0 .. c0 + 63, bf16 pairs
+    constexpr bool det = kDet;             // store into this key block's slice instead of adding
+    int rounds = 0;                        // bulk operations issued by this warp
+    uint32_t pk[16];                       // P for columns c0 .. c0 + 31, bf16 pairs
     uint32_t dq[kCols];                    // drained dQ of the previous query block
     float* dq_dst = nullptr;               // its first unit in the accumulator
-    bool pending = false;                  // reductions of dq still to issue
+    bool pending_lo = false, pending_hi = false;
 
-    constexpr bool det = kDet;             // store into this key block's slice instead of adding
-    auto issue_reds = [&](auto m0c) {      // reductions m0 .. m0 + kRedsQuarter - 1
+    auto issue_reds = [&](auto m0c) {      // 16-byte pieces m0 .. m0 + kRedsHalf - 1 of dq
       constexpr int m0 = decltype(m0c)::value;
 #pragma unroll
-      for (int m = m0; m < m0 + kRedsQuarter; ++m) {
+      for (int m = m0; m < m0 + kRedsHalf; ++m) {
         float* a = dq_dst + (m / 4) * kDqUnitFloats + (m % 4) * 128 + lane * 4;
         if (det)
           ptx::st_global_v4(a, __uint_as_float(dq[4 * m]), __uint_as_float(dq[4 * m + 1]),
@@ -429,20 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                           __uint_as_float(dq[4 * m + 2]), __uint_as_float(dq[4 * m + 3]));
       }
     };
-    using Q0 = std::integral_constant<int, 0>;
-    using Q1 = std::integral_constant<int, kRedsQuarter>;
-    using Q2 = std::integral_constant<int, 2 * kRedsQuarter>;
-    using Q3 = std::integral_constant<int, 3 * kRedsQuarter>;
+    using Lo = std::integral_constant<int, 0>;
+    using Hi = std::integral_constant<int, kRedsHalf>;
 
     // dQ(it): TMEM -> registers, then the TMEM columns are released.
     auto drain_dq = [&](int it) -> bool {
       if (!warp_wait(bar(DQ_FULL), it & 1, W)) return false;
       ptx::tc_fence_after();
-      if constexpr (kCols == 64) {
-        ptx::tmem_ld64(tm + Ly::kColdQ + lane_off + G * 64, tm + Ly::kColdQ + lane_off + G * 64 + 32,
-                       *reinterpret_cast<uint32_t(*)[64]>(dq));
-      } else {
+      if constexpr (kCols == 32) {
         ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(dq));
+      } else {
+        ptx::tmem_ld16(tm + Ly::kColdQ + lane_off + G * 16, *reinterpret_cast<uint32_t(*)[16]>(dq));
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DQ_EMPTY));
@@ -468,13 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::bulk_commit();
         }
         ++rounds;
-      } else if (kSplitReds) {
-        pending = true;
       } else {
-        issue_reds(Q0{});
-        issue_reds(Q1{});
-        issue_reds(Q2{});
-        issue_reds(Q3{});
+        pending_lo = pending_hi = true;
       }
       return true;
     };
@@ -484,117 +467,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = i & 1;
       const uint32_t ph = i & 1;
       const int q0 = (q_first + i) * kBlk;
-      // ---- P(i); the second half of the pending reductions goes between its halves
+      // ---- P(i)
       if (!(ok = warp_wait(bar(S_FULL), ph, W))) break;
       if (!(ok = warp_wait(bar(QFULL0 + st), (i >> 1) & 1, W))) break;
       ptx::tc_fence_after();
       {
+        uint32_t r[32];
+        ptx::tmem_ld32(tm + Ly::kColS + lane_off + c0, r);
         const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4 + c0 * 4;
         const bool diag = prm.causal && q0 == k0;
 #pragma unroll
-        for (int hf = 0; hf < kHalves; ++hf) {
-          uint32_t r[kW];
-          tmem_ld_cols(tm + Ly::kColS + lane_off + c0 + kW * hf, r);
-#pragma unroll
-          for (int j = 0; j < kW; j += 4) {
-            const float4 l4 = ptx::ld_shared_f4(sLa + (kW * hf + j) * 4);
-            float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
-            float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
-            float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
-            float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
-            if (diag) {  // key k0 + t is visible to query q0 + col iff t <= col
-              const int col = c0 + kW * hf + j;
-              p0 = col + 0 < t ? 0.f : p0;
-              p1 = col + 1 < t ? 0.f : p1;
-              p2 = col + 2 < t ? 0.f : p2;
-              p3 = col + 3 < t ? 0.f : p3;
-            }
-            pk[kW / 2 * hf + j / 2] = ptx::pack_bf16x2(p0, p1);
-            pk[kW / 2 * hf + j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+        for (int j = 0; j < 32; j += 4) {
+          const float4 l4 = ptx::ld_shared_f4(sLa + j * 4);
+          float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
+          float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
+          float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
+          float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
+          if (diag) {  // key k0 + t is visible to query q0 + col iff t <= col
+            const int col = c0 + j;
+            p0 = col + 0 < t ? 0.f : p0;
+            p1 = col + 1 < t ? 0.f : p1;
+            p2 = col + 2 < t ? 0.f : p2;
+            p3 = col + 3 < t ? 0.f : p3;
           }
-          if (kSplitReds && pending) {
-            if (hf == 0) issue_reds(Q2{});
-            else issue_reds(Q3{});
-          }
+          pk[j / 2] = ptx::pack_bf16x2(p0, p1);
+          pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
         }
-        if (kSplitReds) pending = false;
         if (!key_ok) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) pk[k] = 0u;
+          for (int k = 0; k < 16; ++k) pk[k] = 0u;
         }
-        ptx::tmem_st16(tm + Ly::kColS + lane_off + G * 64, &pk[0]);
-        ptx::tmem_st16(tm + Ly::kColS + lane_off + G * 64 + 16, &pk[16]);
+        // P columns [c0, c0 + 16) lie over this warp's own S columns
+        ptx::tmem_st16(tm + Ly::kColS + lane_off + c0, &pk[0]);
         ptx::tmem_st_wait();
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(P_FULL));
+      if (pending_hi) {
+        issue_reds(Hi{});
+        pending_hi = false;
+      }
       // ---- dQ(i-1); also guarantees dS(i-1) has been consumed
       if (i > 0 && !(ok = drain_dq(i - 1))) break;
-      // ---- dS(i); the first half of dQ(i-1)'s reductions goes between its halves
+      // ---- dS(i)
       if (!(ok = warp_wait(bar(DP_FULL), ph, W))) break;
       ptx::tc_fence_after();
       {
+        uint32_t r[32];
+        ptx::tmem_ld32(tm + Ly::kColdP + lane_off + c0, r);
         const uint32_t sDa = sbase + Ly::kD + st * kBlk * 4 + c0 * 4;
-        // row t of dS^T, query columns [c0, c0 + 64) = chunk G: eight 16-byte
-        // pieces, 128-byte swizzle (piece index XOR row % 8)
-        const uint32_t row = sdS + G * Ly::kChunk + t * 128;
+        uint32_t ds[16];
 #pragma unroll
-        for (int hf = 0; hf < kHalves; ++hf) {
-          uint32_t r[kW];
-          tmem_ld_cols(tm + Ly::kColdP + lane_off + c0 + kW * hf, r);
-          uint32_t ds[kW / 2];
+        for (int j = 0; j < 32; j += 4) {
+          // dS = P * (dP - D): the difference in fp32 (dP and D nearly
+          // cancel), then one bf16x2 product with the packed bf16 P
+          const float4 d4 = ptx::ld_shared_f4(sDa + j * 4);
+          const uint32_t g01 = ptx::pack_bf16x2(__uint_as_float(r[j + 0]) - d4.x, __uint_as_float(r[j + 1]) - d4.y);
+          const uint32_t g23 = ptx::pack_bf16x2(__uint_as_float(r[j + 2]) - d4.z, __uint_as_float(r[j + 3]) - d4.w);
+          ds[j / 2] = ptx::mul_bf16x2(pk[j / 2], g01);
+          ds[j / 2 + 1] = ptx::mul_bf16x2(pk[j / 2 + 1], g23);
+        }
+        // row t of dS^T, query columns [c0, c0 + 32): chunk G / 2, 16-byte
+        // pieces 4 * (G % 2) .. +3, 128-byte swizzle (piece XOR row % 8)
+        const uint32_t row = sdS + (G >> 1) * Ly::kChunk + t * 128;
 #pragma unroll
-          for (int j = 0; j < kW; j += 4) {
-            // dS = P * (dP - D): the difference in fp32 (dP and D nearly
-            // cancel), then one bf16x2 product with the packed bf16 P
-            const float4 d4 = ptx::ld_shared_f4(sDa + (kW * hf + j) * 4);
-            const uint32_t g01 = ptx::pack_bf16x2(__uint_as_float(r[j + 0]) - d4.x, __uint_as_float(r[j + 1]) - d4.y);
-            const uint32_t g23 = ptx::pack_bf16x2(__uint_as_float(r[j + 2]) - d4.z, __uint_as_float(r[j + 3]) - d4.w);
-            ds[j / 2] = ptx::mul_bf16x2(pk[kW / 2 * hf + j / 2], g01);
-            ds[j / 2 + 1] = ptx::mul_bf16x2(pk[kW / 2 * hf + j / 2 + 1], g23);
-          }
-#pragma unroll
-          for (int u = 0; u < kW / 8; ++u) {
-            const uint32_t piece = (uint32_t)(kW / 8 * hf + u);
-            ptx::st_shared_v4(row + ((piece ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1], ds[4 * u + 2],
-                              ds[4 * u + 3]);
-          }
-          if (pending) {
-            if (hf == 0) issue_reds(Q0{});
-            else issue_reds(Q1{});
-          }
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t piece = (uint32_t)((G & 1) * 4 + u);
+          ptx::st_shared_v4(row + ((piece ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1], ds[4 * u + 2],
+                            ds[4 * u + 3]);
         }
       }
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DS_FULL));
+      if (pending_lo) {
+        issue_reds(Lo{});
+        pending_lo = false;
+      }
     }
-    if (ok && pending) {  // second half of dQ(n-2)
-      issue_reds(Q2{});
-      issue_reds(Q3{});
-      pending = false;
-    }
+    if (ok && pending_hi) issue_reds(Hi{});
+    pending_hi = false;
     if (ok && n_iter > 0) ok = drain_dq(n_iter - 1);
-    if (ok && pending) {
-      issue_reds(Q0{});
-      issue_reds(Q1{});
-      issue_reds(Q2{});
-      issue_reds(Q3{});
+    if (ok && pending_lo) {
+      issue_reds(Lo{});
+      issue_reds(Hi{});
     }
-    if (lane == 0) ptx::bulk_wait_all();  // this warp's bulk reductions are complete
+    if (lane == 0) ptx::bulk_wait_all();  // this warp's bulk operations are complete
     __syncwarp();
     if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
       ptx::tc_fence_after();
-      if (G == 0)
-        store_row<HD>(tm + Ly::kColdV + lane_off, key_ok, prm.dV + head + (int64_t)kr * prm.sn, 1.0f);
+      constexpr int kHalf = HD / 2;        // warps G = 0, 1 store dV, G = 2, 3 store dK
+      const int cc = (G & 1) * kHalf;
+      if (G < 2)
+        store_row<kHalf>(tm + Ly::kColdV + lane_off + cc, key_ok, prm.dV + head + (int64_t)kr * prm.sn + cc, 1.0f);
       else
-        store_row<HD>(tm + Ly::kColdK + lane_off, key_ok, prm.dK + head + (int64_t)kr * prm.sn, prm.scale);
+        store_row<kHalf>(tm + Ly::kColdK + lane_off + cc, key_ok, prm.dK + head + (int64_t)kr * prm.sn + cc,
+                         prm.scale);
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tm, Ly::kTmemCols);
   }
