@@ -395,17 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Reductions issued on the MMA warp's SM sub-partition (lane quarter 1)
     // delay its tcgen05.mma issue, so those four warps stage their dQ share in
     // shared memory and hand it to the TMA unit as one bulk reduction (two
-    // alternating slots per warp).  The other warps keep the drained dQ in
-    // registers and issue its vector reductions in two halves, each right
-    // after the warp has signalled its next dS and P results, so they stay
-    // off the path to those barriers.
+    // alternating slots per warp).  The other warps issue vector reductions
+    // from registers: at d = 128 in two halves, each right after the warp has
+    // signalled its next dS and P results; at d = 64 (half the work per
+    // block) right after the drain, while the warps wait for dV and dP.
+    constexpr bool kSplit = HD == 128;
     const bool staged = qq == 1;
     constexpr bool det = kDet;             // store into this key block's slice instead of adding
     int rounds = 0;                        // bulk operations issued by this warp
     uint32_t pk[16];                       // P for columns c0 .. c0 + 31, bf16 pairs
     uint32_t dq[kCols];                    // drained dQ of the previous query block
-    float* dq_dst = nullptr;               // its first unit in the accumulator
     bool pending_lo = false, pending_hi = false;
+    float* dq_dst = nullptr;               // its first unit in the accumulator
 
     auto issue_reds = [&](auto m0c) {      // 16-byte pieces m0 .. m0 + kRedsHalf - 1 of dq
       constexpr int m0 = decltype(m0c)::value;
@@ -456,8 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::bulk_commit();
         }
         ++rounds;
-      } else {
+      } else if (kSplit) {
         pending_lo = pending_hi = true;
+      } else {
+        issue_reds(Lo{});
+        issue_reds(Hi{});
       }
       return true;
     };
