@@ -7,9 +7,13 @@
 //
 // One CTA owns a 128-row query block (resident in shared memory) and walks
 // the key blocks it can see (all, or up to the diagonal under the causal
-// mask).  S = Q K_b^T goes to one of two TMEM buffers (so S_{b+1} is computed
-// while S_b is turned into P_b); P_b (bf16) is written over S_b and feeds
-// O += P_b V_b straight from TMEM; O accumulates in TMEM.
+// mask).  S_b = Q K_b^T goes to one of three TMEM buffers; P_b (bf16) is
+// written over S_b and feeds O += P_b V_b straight from TMEM; O accumulates
+// in TMEM.  With three buffers S_{b+2} is queued right behind O += P_b V_b
+// (its buffer held P_{b-1}, whose product is already done), so the tensor
+// pipe always has the next score block in hand while the softmax warps work.
+// K lives in three shared-memory stages, each freed as soon as its S block
+// is done; V in two, each freed when its O += P V is done.
 //
 // The exponent base m is only moved when a row maximum grows by more than
 // 2^8 (in exp2 units): otherwise P = exp2(S - m) <= 256 stays well inside
@@ -17,13 +21,14 @@
 // on those rare steps.  The final O / l and L = m + log l are exact for any
 // base.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-7  softmax.  Warp w owns query rows 32*(w%4) .. +31 (its TMEM lane
 //              quarter) and key columns [64*(w/4), +64) of each block; the two
 //              warps of a lane quarter exchange row maxima through shared
 //              memory.  Epilogue: O columns [d/2 * (w/4), +d/2) and L.
-//   warp  8    TMA producer: Q once, K and V double-buffered.
+//   warp  8    TMA producer of Q (once) and K.
 //   warp  9    TMEM allocator and MMA issuer (one elected lane).
+//   warp 10    TMA producer of V.
 //
 // Every wait is bounded (same mechanism as the backward kernel).
 
@@ -44,24 +49,26 @@ bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p); 
 namespace {
 
 constexpr int kBlk = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
+constexpr int kKStages = 3;  // K tiles in shared memory
+constexpr int kVStages = 2;  // V tiles in shared memory
+constexpr int kSBufs = 3;    // S/P buffers in TMEM
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum BarId {
   Q_FULL = 0,
-  KV_FULL0,   // K, V stage landed
-  KV_FULL1,
-  KV_EMPTY0,  // K, V stage free again
-  KV_EMPTY1,
-  S_FULL0,    // S_b in TMEM buffer 0
-  S_FULL1,
-  P_FULL0,    // P_b in TMEM buffer 0 (256 arrivals)
-  P_FULL1,
-  O_DONE,     // O += P_b V_b done
-  DRAIN,      // every MMA done (waited only when a CTA gives up)
+  K_FULL0,                    // K stage landed (kKStages)
+  K_EMPTY0 = K_FULL0 + kKStages,   // K stage read by its S block
+  V_FULL0 = K_EMPTY0 + kKStages,   // V stage landed (kVStages)
+  V_EMPTY0 = V_FULL0 + kVStages,   // V stage read by its O += P V
+  S_FULL0 = V_EMPTY0 + kVStages,   // S_b in TMEM buffer b % 3
+  P_FULL0 = S_FULL0 + kSBufs,      // P_b in TMEM buffer b % 3 (256 arrivals)
+  PV_DONE0 = P_FULL0 + kSBufs,     // O += P_b V_b done: buffer b % 3 free
+  O_DONE = PV_DONE0 + kSBufs,      // O += P_b V_b done (every block)
+  DRAIN,                      // every MMA done (waited only when a CTA gives up)
   kNumBars
 };
 
@@ -70,14 +77,15 @@ struct FwdLayout {
   static constexpr int kChunk = kBlk * 128;
   static constexpr int kTile = kBlk * HD * 2;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;          // 2 stages
-  static constexpr int kV = kK + 2 * kTile;      // 2 stages
-  static constexpr int kX = kV + 2 * kTile;      // exchange: [2 parities (max) + 1 (sum)][2 halves][128] fp32
+  static constexpr int kK = kQ + kTile;                 // kKStages tiles
+  static constexpr int kV = kK + kKStages * kTile;      // kVStages tiles
+  static constexpr int kX = kV + kVStages * kTile;      // exchange: [2 parities (max) + 1 (sum)][2 halves][128] fp32
   static constexpr int kBar = kX + 3 * 2 * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+  static constexpr uint32_t kColO = kSBufs * 128;     // S/P buffers at 0, 128, 256
   static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColO + HD <= kTmemCols, "tensor memory budget");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -118,17 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + Ly::kBar + 8 * i; };
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(bar(Q_FULL), 1);
-    ptx::mbar_init(bar(KV_FULL0), 1);
-    ptx::mbar_init(bar(KV_FULL1), 1);
-    ptx::mbar_init(bar(KV_EMPTY0), 1);
-    ptx::mbar_init(bar(KV_EMPTY1), 1);
-    ptx::mbar_init(bar(S_FULL0), 1);
-    ptx::mbar_init(bar(S_FULL1), 1);
-    ptx::mbar_init(bar(P_FULL0), kSoftmaxThreads);
-    ptx::mbar_init(bar(P_FULL1), kSoftmaxThreads);
-    ptx::mbar_init(bar(O_DONE), 1);
-    ptx::mbar_init(bar(DRAIN), 1);
+    for (int i = 0; i < kNumBars; ++i)
+      ptx::mbar_init(bar(i), (i >= P_FULL0 && i < P_FULL0 + kSBufs) ? kSoftmaxThreads : 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -154,39 +153,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sK = [&](int st) -> uint32_t { return sbase + Ly::kK + st * Ly::kTile; };
   auto sV = [&](int st) -> uint32_t { return sbase + Ly::kV + st * Ly::kTile; };
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
+  if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ producers
+    // warp 8: Q once, then K_b into stage b % 3 once S_{b-3} has read it;
+    // warp 10: V_b into stage b % 2 once O += P_{b-2} V_{b-2} has read it
+    const bool isK = warp == 8;
+    const int nst = isK ? kKStages : kVStages;
+    const int full0 = isK ? K_FULL0 : V_FULL0, empty0 = isK ? K_EMPTY0 : V_EMPTY0;
+    const CUtensorMap* map = isK ? &tmK : &tmV;
     bool ok = true;
     int issued = 0;
     if (lane == 0) {
-      ptx::prefetch_tensormap(&tmQ);
-      ptx::prefetch_tensormap(&tmK);
-      ptx::prefetch_tensormap(&tmV);
-      ptx::mbar_arrive_expect_tx(bar(Q_FULL), Ly::kTile);
+      ptx::prefetch_tensormap(map);
+      if (isK) {
+        ptx::prefetch_tensormap(&tmQ);
+        ptx::mbar_arrive_expect_tx(bar(Q_FULL), Ly::kTile);
 #pragma unroll
-      for (int c = 0; c < HD / 64; ++c) ptx::tma_load_4d(sQ + c * Ly::kChunk, &tmQ, bar(Q_FULL), c * 64, q0, h, b);
+        for (int c = 0; c < HD / 64; ++c) ptx::tma_load_4d(sQ + c * Ly::kChunk, &tmQ, bar(Q_FULL), c * 64, q0, h, b);
+      }
     }
     for (int j = 0; j < n_blk; ++j) {
-      const int st = j & 1;
-      if (j >= 2 && !(ok = warp_wait(bar(KV_EMPTY0 + st), ((j - 2) >> 1) & 1, W))) break;
+      const int st = j % nst;
+      if (j >= nst && !(ok = warp_wait(bar(empty0 + st), ((j - nst) / nst) & 1, W))) break;
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(KV_FULL0 + st), 2 * Ly::kTile);
+        const uint32_t dst = isK ? sK(st) : sV(st);
+        ptx::mbar_arrive_expect_tx(bar(full0 + st), Ly::kTile);
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) {
-          ptx::tma_load_4d(sK(st) + c * Ly::kChunk, &tmK, bar(KV_FULL0 + st), c * 64, j * kBlk, h, b);
-          ptx::tma_load_4d(sV(st) + c * Ly::kChunk, &tmV, bar(KV_FULL0 + st), c * 64, j * kBlk, h, b);
-        }
+        for (int c = 0; c < HD / 64; ++c)
+          ptx::tma_load_4d(dst + c * Ly::kChunk, map, bar(full0 + st), c * 64, j * kBlk, h, b);
       }
       __syncwarp();
       issued = j + 1;
     }
     if (!ok) {
-      ptx::wait_bounded(bar(Q_FULL), 0, W, false);
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-        ptx::wait_bounded(bar(KV_FULL0 + (j & 1)), (j >> 1) & 1, W, false);
+      // shared memory must not be released under copies still in flight
+      if (isK) ptx::wait_bounded(bar(Q_FULL), 0, W, false);
+      for (int j = issued > nst ? issued - nst : 0; j < issued; ++j)
+        ptx::wait_bounded(bar(full0 + j % nst), (j / nst) & 1, W, false);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
+    // order: S_0, S_1, then per block b: O += P_b V_b, S_{b+2}
     constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
     constexpr uint32_t kIdO = ptx::idesc_bf16_f32(128, HD, false, true);    // O += P V
     auto kdesc = [&](uint32_t tile, int kk) -> uint64_t {
@@ -196,48 +203,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
     };
     const uint32_t tO = tm + Ly::kColO;
-    auto issue_S = [&](int j) {
-      const uint32_t tS = tm + ((j & 1) ? Ly::kColS1 : Ly::kColS0);
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS, kdesc(sQ, kk), kdesc(sK(j & 1), kk), kIdS, kk > 0);
-      ptx::tc_commit(bar(S_FULL0 + (j & 1)));
-    };
-    bool ok = warp_wait(bar(Q_FULL), 0, W) && warp_wait(bar(KV_FULL0), 0, W);
-    if (ok) {
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) issue_S(0);
-      __syncwarp();
-    }
-    if (ok && n_blk > 1) {
-      ok = warp_wait(bar(KV_FULL1), 0, W);
-      if (ok) {
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) issue_S(1);
-        __syncwarp();
-      }
-    }
-    for (int j = 0; ok && j < n_blk; ++j) {
-      const int st = j & 1;
-      // O += P_j V_j  (A = P_j from TMEM: key steps 0-3 in columns [0,32), 4-7 in [64,96))
-      if (!(ok = warp_wait(bar(P_FULL0 + st), (j >> 1) & 1, W))) break;
+    // S_j into buffer j % 3 once K_j has landed and (j >= 3) O += P_{j-3} V_{j-3}
+    // has read the buffer
+    auto issue_S = [&](int j) -> bool {
+      const int sb = j % kSBufs, ks = j % kKStages;
+      if (!warp_wait(bar(K_FULL0 + ks), (j / kKStages) & 1, W)) return false;
+      if (j >= kSBufs && !warp_wait(bar(PV_DONE0 + sb), ((j - kSBufs) / kSBufs) & 1, W)) return false;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
-        const uint32_t tP = tm + (st ? Ly::kColS1 : Ly::kColS0);
+        const uint32_t tS = tm + sb * 128;
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          ptx::mma_ts(tO, tP + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(sV(st), kk), kIdO, (j | kk) != 0);
-        ptx::tc_commit(bar(O_DONE));
-        ptx::tc_commit(bar(KV_EMPTY0 + st));
+        for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS, kdesc(sQ, kk), kdesc(sK(ks), kk), kIdS, kk > 0);
+        ptx::tc_commit(bar(S_FULL0 + sb));
+        ptx::tc_commit(bar(K_EMPTY0 + ks));
       }
       __syncwarp();
-      // S_{j+2} into the same TMEM buffer once P_j has been read
-      if (j + 2 < n_blk) {
-        if (!(ok = warp_wait(bar(KV_FULL0 + st), ((j + 2) >> 1) & 1, W))) break;
-        if (!(ok = warp_wait(bar(O_DONE), j & 1, W))) break;
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) issue_S(j + 2);
-        __syncwarp();
+      return true;
+    };
+    bool ok = warp_wait(bar(Q_FULL), 0, W) && issue_S(0);
+    if (ok && n_blk > 1) ok = issue_S(1);
+    for (int j = 0; ok && j < n_blk; ++j) {
+      const int sb = j % kSBufs, vs = j % kVStages;
+      // O += P_j V_j  (A = P_j from TMEM: key steps 0-3 in columns [0,32), 4-7 in [64,96))
+      if (!(ok = warp_wait(bar(P_FULL0 + sb), (j / kSBufs) & 1, W))) break;
+      if (!(ok = warp_wait(bar(V_FULL0 + vs), (j / kVStages) & 1, W))) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        const uint32_t tP = tm + sb * 128;
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          ptx::mma_ts(tO, tP + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(sV(vs), kk), kIdO, (j | kk) != 0);
+        ptx::tc_commit(bar(PV_DONE0 + sb));
+        ptx::tc_commit(bar(O_DONE));
+        ptx::tc_commit(bar(V_EMPTY0 + vs));
       }
+      __syncwarp();
+      if (j + 2 < n_blk) ok = issue_S(j + 2);
     }
     // the softmax warps wait for the last O_DONE; on an abort make sure no
     // MMA is still in flight before tensor memory is freed
@@ -257,25 +258,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_part = 0.f;                    // this warp's part of the row sum
     bool ok = true;
     for (int j = 0; j < n_blk; ++j) {
-      const int st = j & 1;
-      const uint32_t tS = tm + (st ? Ly::kColS1 : Ly::kColS0);
-      if (!(ok = warp_wait(bar(S_FULL0 + st), (j >> 1) & 1, W))) break;
+      const int st = j & 1;            // parity of the row-maximum exchange slot
+      const int sb = j % kSBufs;       // TMEM buffer of S_j / P_j
+      const uint32_t tS = tm + sb * 128;
+      if (!(ok = warp_wait(bar(S_FULL0 + sb), (j / kSBufs) & 1, W))) break;
       ptx::tc_fence_after();
       uint32_t r[64];
       ptx::tmem_ld64(tS + lane_off + c0, tS + lane_off + c0 + 32, r);
       const int k0 = j * kBlk + c0;
-      const bool need_mask = (prm.causal && j == qt) || (j * kBlk + kBlk > prm.N);
-      float mx = -INFINITY;
+      if ((prm.causal && j == qt) || (j * kBlk + kBlk > prm.N)) {
+        // columns c >= lim of this warp's 64 are masked (past N, or later
+        // than the query under the causal mask)
+        int lim = prm.N - k0;
+        if (prm.causal) lim = min(lim, qrow - k0 + 1);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float s = __uint_as_float(r[c]) * sl2;
-        if (need_mask) {
-          const int key = k0 + c;
-          if (key >= prm.N || (prm.causal && key > qrow)) s = -INFINITY;
-        }
-        r[c] = __float_as_uint(s);
-        mx = fmaxf(mx, s);
+        for (int c = 0; c < 64; ++c) r[c] = c < lim ? r[c] : __float_as_uint(-INFINITY);
       }
+      // row maximum of the raw scores (scale > 0 commutes with max), four
+      // independent chains
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r[c]));
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
       // row maximum over both halves of the block
       xchg[(st * 2 + G) * kBlk + t] = mx;
       named_bar_sync(1 + qq, 64);
@@ -311,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float p0 = ptx::ex2(__uint_as_float(r[c]) - mb);
-        const float p1 = ptx::ex2(__uint_as_float(r[c + 1]) - mb);
+        const float p0 = ptx::ex2(fmaf(__uint_as_float(r[c]), sl2, -mb));
+        const float p1 = ptx::ex2(fmaf(__uint_as_float(r[c + 1]), sl2, -mb));
         l_part += p0 + p1;
         pk[c / 2] = ptx::pack_bf16x2(p0, p1);
       }
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_st16(tS + lane_off + G * 64 + 16, &pk[16]);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(P_FULL0 + st));
+      ptx::mbar_arrive(bar(P_FULL0 + sb));
     }
     // epilogue: O / l and L
     if (ok) {
