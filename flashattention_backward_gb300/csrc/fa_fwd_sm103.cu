@@ -9,9 +9,9 @@
 // the key blocks it can see (all, or up to the diagonal under the causal
 // mask).  S_b = Q K_b^T goes to one of three TMEM buffers; P_b (bf16) is
 // written over S_b and feeds O += P_b V_b straight from TMEM; O accumulates
-// in TMEM.  With three buffers S_{b+2} is queued right behind O += P_b V_b
-// (its buffer held P_{b-1}, whose product is already done), so the tensor
-// pipe always has the next score block in hand while the softmax warps work.
+// in TMEM.  With three buffers S_{b+2} is issued as soon as O += P_{b-1} V_{b-1}
+// has read its buffer, ahead of O += P_b V_b, so the tensor pipe computes the
+// score block two ahead while the softmax warps still work on P_b.
 // K lives in three shared-memory stages, each freed as soon as its S block
 // is done; V in two, each freed when its O += P V is done.
 //
@@ -60,15 +60,19 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum BarId {
   Q_FULL = 0,
-  K_FULL0,                    // K stage landed (kKStages)
+  K_FULL0,                         // K stage landed (kKStages)
   K_EMPTY0 = K_FULL0 + kKStages,   // K stage read by its S block
   V_FULL0 = K_EMPTY0 + kKStages,   // V stage landed (kVStages)
   V_EMPTY0 = V_FULL0 + kVStages,   // V stage read by its O += P V
-  S_FULL0 = V_EMPTY0 + kVStages,   // S_b in TMEM buffer b % 3
-  P_FULL0 = S_FULL0 + kSBufs,      // P_b in TMEM buffer b % 3 (256 arrivals)
-  PV_DONE0 = P_FULL0 + kSBufs,     // O += P_b V_b done: buffer b % 3 free
-  O_DONE = PV_DONE0 + kSBufs,      // O += P_b V_b done (every block)
-  DRAIN,                      // every MMA done (waited only when a CTA gives up)
+  S_READY0 = V_EMPTY0 + kVStages,  // S_b may be issued: K_b forwarded by its producer and
+                                   // buffer b % 3 read by O += P_{b-3} V_{b-3} (2 arrivals)
+  S_FULL0 = S_READY0 + kSBufs,     // S_b in TMEM buffer b % 3
+  P_FULL0 = S_FULL0 + kSBufs,      // P_b in buffer b % 3 and V_b forwarded (256 + 1 arrivals)
+  O_DONE0 = P_FULL0 + kSBufs,      // O += P_b V_b (and every MMA before it) done, on
+                                   // barrier b % 3.  The softmax warps ask about block b-1
+                                   // only after S_b, whose commit proves O += P_{b-3} V_{b-3}
+                                   // done, so the parity always names the current phase
+  DRAIN = O_DONE0 + kSBufs,        // every MMA done (waited only when a CTA gives up)
   kNumBars
 };
 
@@ -127,7 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      ptx::mbar_init(bar(i), (i >= P_FULL0 && i < P_FULL0 + kSBufs) ? kSoftmaxThreads : 1);
+      ptx::mbar_init(bar(i), (i >= P_FULL0 && i < P_FULL0 + kSBufs)     ? kSoftmaxThreads + 1
+                             : (i >= S_READY0 && i < S_READY0 + kSBufs) ? 2
+                                                                        : 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -156,13 +162,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ producers
     // warp 8: Q once, then K_b into stage b % 3 once S_{b-3} has read it;
-    // warp 10: V_b into stage b % 2 once O += P_{b-2} V_{b-2} has read it
+    // warp 10: V_b into stage b % 2 once O += P_{b-2} V_{b-2} has read it.
+    // Each producer waits for its own copies and forwards their completion
+    // (K_b to S_READY, V_b to P_FULL), so the MMA warp waits on two
+    // barriers per block.  Forwarding block b-1 after issuing block b keeps
+    // one copy in flight while the previous one is confirmed.
     const bool isK = warp == 8;
     const int nst = isK ? kKStages : kVStages;
     const int full0 = isK ? K_FULL0 : V_FULL0, empty0 = isK ? K_EMPTY0 : V_EMPTY0;
     const CUtensorMap* map = isK ? &tmK : &tmV;
+    auto forward = [&](int j) -> bool {
+      if (!warp_wait(bar(full0 + j % nst), (j / nst) & 1, W)) return false;
+      if (lane == 0) {
+        if (isK) {
+          ptx::mbar_arrive(bar(S_READY0 + j % kSBufs));
+          if (j < kSBufs) ptx::mbar_arrive(bar(S_READY0 + j));  // no earlier reader of the buffer
+        } else {
+          ptx::mbar_arrive(bar(P_FULL0 + j % kSBufs));
+        }
+      }
+      __syncwarp();
+      return true;
+    };
     bool ok = true;
-    int issued = 0;
+    int issued = 0, forwarded = 0;
     if (lane == 0) {
       ptx::prefetch_tensormap(map);
       if (isK) {
@@ -184,16 +207,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       issued = j + 1;
+      if (j >= 1) {
+        if (!(ok = forward(j - 1))) break;
+        forwarded = j;
+      }
+    }
+    if (ok && issued > 0) {
+      if ((ok = forward(issued - 1))) forwarded = issued;
     }
     if (!ok) {
       // shared memory must not be released under copies still in flight
       if (isK) ptx::wait_bounded(bar(Q_FULL), 0, W, false);
-      for (int j = issued > nst ? issued - nst : 0; j < issued; ++j)
-        ptx::wait_bounded(bar(full0 + j % nst), (j / nst) & 1, W, false);
+      for (int j = forwarded; j < issued; ++j) ptx::wait_bounded(bar(full0 + j % nst), (j / nst) & 1, W, false);
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
-    // order: S_0, S_1, then per block b: O += P_b V_b, S_{b+2}
+    // order: S_0, S_1, then per block b: S_{b+2}, O += P_b V_b
     constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
     constexpr uint32_t kIdO = ptx::idesc_bf16_f32(128, HD, false, true);    // O += P V
     auto kdesc = [&](uint32_t tile, int kk) -> uint64_t {
@@ -207,8 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // has read the buffer
     auto issue_S = [&](int j) -> bool {
       const int sb = j % kSBufs, ks = j % kKStages;
-      if (!warp_wait(bar(K_FULL0 + ks), (j / kKStages) & 1, W)) return false;
-      if (j >= kSBufs && !warp_wait(bar(PV_DONE0 + sb), ((j - kSBufs) / kSBufs) & 1, W)) return false;
+      if (!warp_wait(bar(S_READY0 + sb), (j / kSBufs) & 1, W)) return false;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
         const uint32_t tS = tm + sb * 128;
@@ -224,21 +252,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n_blk > 1) ok = issue_S(1);
     for (int j = 0; ok && j < n_blk; ++j) {
       const int sb = j % kSBufs, vs = j % kVStages;
+      // S_{j+2} first: it only waits for O += P_{j-1} V_{j-1}, so the score
+      // block two ahead is in flight while the softmax warps finish P_j
+      if (j + 2 < n_blk && !(ok = issue_S(j + 2))) break;
       // O += P_j V_j  (A = P_j from TMEM: key steps 0-3 in columns [0,32), 4-7 in [64,96))
-      if (!(ok = warp_wait(bar(P_FULL0 + sb), (j / kSBufs) & 1, W))) break;
-      if (!(ok = warp_wait(bar(V_FULL0 + vs), (j / kVStages) & 1, W))) break;
+      if (!(ok = warp_wait(bar(P_FULL0 + sb), (j / kSBufs) & 1, W))) break;  // P_j and V_j
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
         const uint32_t tP = tm + sb * 128;
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
           ptx::mma_ts(tO, tP + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(sV(vs), kk), kIdO, (j | kk) != 0);
-        ptx::tc_commit(bar(PV_DONE0 + sb));
-        ptx::tc_commit(bar(O_DONE));
+        ptx::tc_commit(bar(S_READY0 + sb));  // buffer free for S_{j+3}
+        ptx::tc_commit(bar(O_DONE0 + sb));
         ptx::tc_commit(bar(V_EMPTY0 + vs));
       }
       __syncwarp();
-      if (j + 2 < n_blk) ok = issue_S(j + 2);
     }
     // the softmax warps wait for the last O_DONE; on an abort make sure no
     // MMA is still in flight before tensor memory is freed
@@ -292,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // O (this warp's columns) and l move to the new base: O *= 2^(m - m')
-        if (!(ok = warp_wait(bar(O_DONE), (j - 1) & 1, W))) break;
+        if (!(ok = warp_wait(bar(O_DONE0 + (j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, W))) break;
         ptx::tc_fence_after();
         const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.f;
         constexpr int kOC = HD / 2;
@@ -331,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       xchg[(4 + G) * kBlk + t] = l_part;
       named_bar_sync(1 + qq, 64);
       const float l = l_part + xchg[(4 + (G ^ 1)) * kBlk + t];
-      if (warp_wait(bar(O_DONE), (n_blk - 1) & 1, W)) {
+      if (warp_wait(bar(O_DONE0 + (n_blk - 1) % kSBufs), ((n_blk - 1) / kSBufs) & 1, W)) {
         ptx::tc_fence_after();
         const float inv = 1.f / l;
         constexpr int kOC = HD / 2;
