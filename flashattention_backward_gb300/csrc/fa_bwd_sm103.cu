@@ -21,9 +21,9 @@
 //              latencies).
 //              Per query block: P = exp2(S*scale*log2e - L*log2e) -> bf16
 //              into TMEM; dQ of the previous block TMEM -> registers ->
-//              fp32 reductions into global (vector reductions, or a bulk
-//              reduction through shared memory for the warps that share an
-//              SM sub-partition with the MMA warp); dS = P * (dP - D) -> bf16
+//              fp32 reductions into global (a bulk reduction staged through
+//              shared memory where it has room, else vector reductions from
+//              registers); dS = P * (dP - D) -> bf16
 //              into shared memory (128-byte swizzle).  Epilogue: dV (w < 8)
 //              and scale * dK (w >= 8), half the columns each.
 //   warp 16    TMA producer: K, V once; Q (two stages, with its L and D rows)
@@ -101,8 +101,11 @@ struct Layout {
   static constexpr int kQ = kV + kTile;                 // 2 stages
   static constexpr int kdO = kQ + 2 * kTile;            // kDoStages stages
   static constexpr int kdS = kdO + kDoStages * kTile;   // 128 x 128 bf16, two 64-column chunks
-  static constexpr int kStage = kdS + 2 * kChunk;       // dQ staging of lane quarter 1: 2 warps x 2 slots
-  static constexpr int kL = kStage + 2 * 2 * (HD / 32) * 2048;  // 2 stages x 128 fp32 (L * log2 e)
+  // dQ staging for bulk reductions: lane quarters 0 and 1, one slot of
+  // 32 x d/4 fp32 per warp
+  static constexpr int kStage = kdS + 2 * kChunk;
+  static constexpr int kStageBytes = 8 * 32 * (HD / 4) * 4;
+  static constexpr int kL = kStage + kStageBytes;      // 2 stages x 128 fp32 (L * log2 e)
   static constexpr int kD = kL + 2 * kBlk * 4;          // 2 stages x 128 fp32
   static constexpr int kBar = kD + 2 * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
@@ -392,15 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kCols = HD / 4;          // this warp's dQ columns [G * kCols, +kCols)
     constexpr int kUnits = kCols / 16;     // 2 KB units, contiguous in the accumulator
     constexpr int kRedsHalf = kCols / 8;   // 16-byte reductions per lane per query block, halved
-    // Reductions issued on the MMA warp's SM sub-partition (lane quarter 1)
-    // delay its tcgen05.mma issue, so those four warps stage their dQ share in
-    // shared memory and hand it to the TMA unit as one bulk reduction (two
-    // alternating slots per warp).  The other warps issue vector reductions
-    // from registers: at d = 128 in two halves, each right after the warp has
-    // signalled its next dS and P results; at d = 64 (half the work per
+    // Vector reductions from registers queue in the SM sub-partition's memory
+    // pipe ahead of the warp's own shared-memory loads, barrier waits and
+    // arrivals (and, on lane quarter 1, delay the MMA warp's tcgen05.mma
+    // issue).  So the warps of lane quarters 0 and 1 (as many as the shared
+    // memory left at d = 128 holds) stage their dQ share there and hand it
+    // to the TMA unit as one bulk reduction, one slot per warp: the operation
+    // issued one query block earlier has long read it.  The other warps issue
+    // vector reductions: at d = 128 in two halves, each right after the warp
+    // has signalled its next dS and P results; at d = 64 (half the work per
     // block) right after the drain, while the warps wait for dV and dP.
     constexpr bool kSplit = HD == 128;
-    const bool staged = qq == 1;
+    const bool staged = qq <= 1;
     constexpr bool det = kDet;             // store into this key block's slice instead of adding
     int rounds = 0;                        // bulk operations issued by this warp
     uint32_t pk[16];                       // P for columns c0 .. c0 + 31, bf16 pairs
@@ -438,8 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       dq_dst = prm.dq_accum + (det ? kb * prm.slice_elems : 0) +
                dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * kUnits, HD);
       if (staged) {
-        const uint32_t buf = sbase + Ly::kStage + G * (2 * kUnits * 2048) + (rounds & 1) * (kUnits * 2048);
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        // one slot per warp, free once the operation issued one query block
+        // earlier has read it
+        const uint32_t buf = sbase + Ly::kStage + (qq * 4 + G) * (kUnits * 2048);
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncwarp();
 #pragma unroll
         for (int u = 0; u < kUnits; ++u)
