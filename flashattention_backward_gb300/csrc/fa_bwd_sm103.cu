@@ -137,6 +137,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const p
   return __all_sync(0xffffffffu, ptx::wait_bounded(bar, parity, w, true));
 }
 
+// Two barriers at once: both are queried back to back, so when both phases
+// are already complete (the usual case for the second) the warp pays one
+// shared-memory round trip instead of two.
+__device__ __forceinline__ bool warp_wait2(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb,
+                                           const ptx::Waiter& w) {
+  const bool done = (ptx::mbar_try_wait(a, pa) & ptx::mbar_try_wait(b, pb)) != 0;
+  if (__all_sync(0xffffffffu, done)) return true;
+  return __all_sync(0xffffffffu, ptx::wait_bounded(a, pa, w, true) && ptx::wait_bounded(b, pb, w, true));
+}
+
 // NC fp32 columns of this thread's TMEM lane -> bf16 in global.
 template <int NC>
 __device__ __forceinline__ void store_row(uint32_t taddr, bool valid, __nv_bfloat16* dst, float mul) {
@@ -480,8 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ph = i & 1;
       const int q0 = (q_first + i) * kBlk;
       // ---- P(i)
-      if (!(ok = warp_wait(bar(S_FULL), ph, W))) break;
-      if (!(ok = warp_wait(bar(QFULL0 + st), (i >> 1) & 1, W))) break;
+      if (!(ok = warp_wait2(bar(S_FULL), ph, bar(QFULL0 + st), (i >> 1) & 1, W))) break;  // S(i); L(i) rows
       ptx::tc_fence_after();
       {
         uint32_t r[32];
