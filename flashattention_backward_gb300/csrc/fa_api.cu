@@ -81,7 +81,11 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ O
                                                          int tiles_per_head, int zero_slices,
                                                          int64_t slice_elems) {
   constexpr int kVec = Vec16<T>::kElems;
-  constexpr int kLanesPerRow = HD / kVec;          // 4 .. 32, a power of two
+  constexpr int kVecs = HD / kVec;                 // 16-byte vectors per row: 2 .. 64
+  // lanes per row: a power of two (lanes past kVecs idle), at most 32; each
+  // lane takes vectors sub, sub + kLanesPerRow, ...
+  constexpr int kLanesPerRow = kVecs <= 2 ? 2 : kVecs <= 4 ? 4 : kVecs <= 8 ? 8 : kVecs <= 16 ? 16 : 32;
+  constexpr int kPerLane = (kVecs + kLanesPerRow - 1) / kLanesPerRow;
   constexpr int kRowsPerStep = 256 / kLanesPerRow;
   constexpr int kSteps = kTileRows / kRowsPerStep;
   const int tile = blockIdx.x % tiles_per_head;
@@ -96,11 +100,15 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ O
   for (int s = 0; s < kSteps; ++s) {
     const int n = tile * kTileRows + s * kRowsPerStep + row_in_step;
     acc[s] = 0.f;
-    if (n < N) {
-      const int64_t off = head_off + (int64_t)n * sn + sub * kVec;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(O + off));
-      const uint4 g = __ldg(reinterpret_cast<const uint4*>(dO + off));
-      acc[s] = Vec16<T>::dot(a, g);
+#pragma unroll
+    for (int v = 0; v < kPerLane; ++v) {
+      const int vec = sub + v * kLanesPerRow;
+      if (n < N && vec < kVecs) {
+        const int64_t off = head_off + (int64_t)n * sn + vec * kVec;
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(O + off));
+        const uint4 g = __ldg(reinterpret_cast<const uint4*>(dO + off));
+        acc[s] += Vec16<T>::dot(a, g);
+      }
     }
   }
 #pragma unroll
@@ -125,10 +133,11 @@ static cudaError_t launch_preprocess_t(const fa_problem& p, const T* O, const T*
                                        cudaStream_t s) {
   const int tiles = (int)ceil_div(p.N, kTileRows);
   const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
-  // Deterministic bf16: every slice element the convert reads is written by
-  // the backward kernel, so nothing needs zeroing.  Deterministic fp32: the
-  // 64-row kernel leaves parts of some slices untouched; zero them all.
-  const int zero_slices = !deterministic(p) ? 1 : (p.dtype == FA_BF16 ? 0 : (int)dq_slices(p));
+  // Deterministic, tensor-core kernel: every slice element the convert reads
+  // is written by the backward kernel, so nothing needs zeroing.  The
+  // CUDA-core kernel's 64- or 32-row key blocks leave parts of some slices
+  // untouched; zero them all.
+  const int zero_slices = !deterministic(p) ? 1 : (tensor_core(p) ? 0 : (int)dq_slices(p));
   const int64_t slice_elems = dq_slice_elems(p);
 #define FA_PRE_CASE(HDV)                                                                                    \
   case HDV:                                                                                                 \
@@ -139,7 +148,9 @@ static cudaError_t launch_preprocess_t(const fa_problem& p, const T* O, const T*
     FA_PRE_CASE(16)
     FA_PRE_CASE(32)
     FA_PRE_CASE(64)
+    FA_PRE_CASE(96)
     FA_PRE_CASE(128)
+    FA_PRE_CASE(256)
     default:
       return cudaErrorInvalidValue;
   }
@@ -244,7 +255,9 @@ static cudaError_t launch_convert_t(const fa_problem& p, const float* acc, T* dQ
     FA_CONV_CASE(16)
     FA_CONV_CASE(32)
     FA_CONV_CASE(64)
+    FA_CONV_CASE(96)
     FA_CONV_CASE(128)
+    FA_CONV_CASE(256)
     default:
       return cudaErrorInvalidValue;
   }
@@ -302,9 +315,10 @@ fa_status validate(const fa_problem* p) {
   if (p->stride_n < p->d || p->stride_h < 1 || p->stride_b < 1) return FA_ERR_INVALID_ARG;
   if ((p->stride_n * es) % 16 || (p->stride_h * es) % 16 || (p->stride_b * es) % 16) return FA_ERR_INVALID_ARG;
   if (p->dtype == FA_BF16) {
-    if (p->d != 64 && p->d != 128) return FA_ERR_UNSUPPORTED;
+    if (p->d != 32 && p->d != 64 && p->d != 96 && p->d != 128 && p->d != 256) return FA_ERR_UNSUPPORTED;
   } else {
-    if (p->d != 16 && p->d != 32 && p->d != 64 && p->d != 128) return FA_ERR_UNSUPPORTED;
+    if (p->d != 16 && p->d != 32 && p->d != 64 && p->d != 96 && p->d != 128 && p->d != 256)
+      return FA_ERR_UNSUPPORTED;
   }
   return FA_OK;
 }
@@ -326,7 +340,7 @@ fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* 
   if (st != FA_OK) return st;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(L)) return FA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (p->dtype == FA_FP32) return from_cuda(fa::launch_fwd_simt(*p, Q, K, V, O, L, s));
+  if (!fa::tensor_core(*p)) return from_cuda(fa::launch_fwd_simt(*p, Q, K, V, O, L, s));
   int32_t* status = fa::device_status_word();
   if (!status) return FA_ERR_CUDA;
   return from_cuda(fa::launch_fwd_sm103(*p, Q, K, V, O, L, status, fa::wait_limit_ns(), s));
@@ -348,9 +362,7 @@ fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* 
       !aligned16(dQ_accum) || !aligned16(dK) || !aligned16(dV))
     return FA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (p->dtype == FA_FP32)
-    return from_cuda(fa::launch_bwd_simt_fp32(*p, (const float*)Q, (const float*)K, (const float*)V,
-                                              (const float*)dO, L, D, dQ_accum, (float*)dK, (float*)dV, s));
+  if (!fa::tensor_core(*p)) return from_cuda(fa::launch_bwd_simt(*p, Q, K, V, dO, L, D, dQ_accum, dK, dV, s));
   int32_t* status = fa::device_status_word();
   if (!status) return FA_ERR_CUDA;
   return from_cuda(fa::launch_bwd_sm103(*p, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s));

@@ -1,4 +1,4 @@
-// FlashAttention-2 backward for bf16, head dim 64 or 128, on the sm_100-family
+// FlashAttention-2 backward for bf16, head dim 32, 64, 96 or 128, on the sm_100-family
 // tensor cores (tcgen05 MMA with accumulators in tensor memory, operands
 // staged in shared memory by TMA).
 //
@@ -34,7 +34,8 @@
 //   [0,128)     S^T; P^T (bf16) is written over it: query columns
 //               [32g, 32g + 32) of S become P columns [32g, 32g + 16)
 //   [128,256)   dP^T, then the dQ tile of the same step written over it
-//   [256,256+d) dV accumulator, [256+d,256+2d) dK accumulator
+//   [256,256+d) dV accumulator, [256+LD,256+LD+d) dK accumulator (LD = 64
+//               for d <= 64, else 128)
 //
 // MMA issue order per query block i (software pipelined):
 //   dV(i)  dP(i)  S(i+1)  dK(i)  dQ(i)
@@ -91,27 +92,30 @@ enum BarId {
   kNumBars
 };
 
-template <int HD>
+// Shared-memory and TMEM layout for tiles LD = 64 or 128 columns wide (head
+// dims 32 and 64 use LD = 64, 96 and 128 use LD = 128; the TMA zero-fills the
+// columns past d).
+template <int LD>
 struct Layout {
-  static constexpr int kDoStages = HD == 128 ? 1 : 2;
+  static constexpr int kDoStages = LD == 128 ? 1 : 2;
   static constexpr int kChunk = kBlk * 128;     // 128 rows x 128 bytes (64 bf16 columns)
-  static constexpr int kTile = kBlk * HD * 2;   // one Q / K / V / dO tile
+  static constexpr int kTile = kBlk * LD * 2;   // one Q / K / V / dO tile
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;                 // 2 stages
   static constexpr int kdO = kQ + 2 * kTile;            // kDoStages stages
   static constexpr int kdS = kdO + kDoStages * kTile;   // 128 x 128 bf16, two 64-column chunks
   // dQ staging for bulk reductions: lane quarters 0 and 1, one slot of
-  // 32 x d/4 fp32 per warp
+  // 32 x LD/4 fp32 per warp
   static constexpr int kStage = kdS + 2 * kChunk;
-  static constexpr int kStageBytes = 8 * 32 * (HD / 4) * 4;
+  static constexpr int kStageBytes = 8 * 32 * (LD / 4) * 4;
   static constexpr int kL = kStage + kStageBytes;      // 2 stages x 128 fp32 (L * log2 e)
   static constexpr int kD = kL + 2 * kBlk * 4;          // 2 stages x 128 fp32
   static constexpr int kBar = kD + 2 * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 128;
-  static constexpr uint32_t kColdV = 256, kColdK = 256 + HD;
+  static constexpr uint32_t kColdV = 256, kColdK = 256 + LD;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -147,24 +151,32 @@ __device__ __forceinline__ bool warp_wait2(uint32_t a, uint32_t pa, uint32_t b, 
   return __all_sync(0xffffffffu, ptx::wait_bounded(a, pa, w, true) && ptx::wait_bounded(b, pb, w, true));
 }
 
-// NC fp32 columns of this thread's TMEM lane -> bf16 in global.
+// NC fp32 columns of this thread's TMEM lane -> bf16 in global (NC a
+// multiple of 16: 32-column pieces, then a 16-column tail).
+__device__ __forceinline__ void store_cols(const uint32_t* r, int n, __nv_bfloat16* dst, float mul) {
+#pragma unroll
+  for (int u = 0; u < n / 8; ++u) {
+    uint4 v;
+    v.x = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 0]) * mul, __uint_as_float(r[8 * u + 1]) * mul);
+    v.y = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul);
+    v.z = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul);
+    v.w = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul);
+    *reinterpret_cast<uint4*>(dst + u * 8) = v;
+  }
+}
 template <int NC>
 __device__ __forceinline__ void store_row(uint32_t taddr, bool valid, __nv_bfloat16* dst, float mul) {
+  static_assert(NC % 16 == 0, "16-column granularity");
 #pragma unroll
   for (int c = 0; c < NC / 32; ++c) {
     uint32_t r[32];
     ptx::tmem_ld32(taddr + c * 32, r);
-    if (valid) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint4 v;
-        v.x = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 0]) * mul, __uint_as_float(r[8 * u + 1]) * mul);
-        v.y = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul);
-        v.z = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul);
-        v.w = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul);
-        *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = v;
-      }
-    }
+    if (valid) store_cols(r, 32, dst + c * 32, mul);
+  }
+  if constexpr (NC % 32 == 16) {
+    uint32_t r[16];
+    ptx::tmem_ld16(taddr + (NC / 32) * 32, r);
+    if (valid) store_cols(r, 16, dst + (NC / 32) * 32, mul);
   }
 }
 
@@ -173,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                      const BwdParams prm) {
-  using Ly = Layout<HD>;
+  constexpr int LD = HD <= 64 ? 64 : 128;
+  using Ly = Layout<LD>;
   constexpr int kDoSt = Ly::kDoStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_addr(smem);
@@ -244,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tensormap(&tmdO);
       ptx::mbar_arrive_expect_tx(bar(KV_FULL), 2 * Ly::kTile);
 #pragma unroll
-      for (int c = 0; c < HD / 64; ++c) {
+      for (int c = 0; c < LD / 64; ++c) {
         ptx::tma_load_4d(sK + c * Ly::kChunk, &tmK, bar(KV_FULL), c * 64, k0, h, b);
         ptx::tma_load_4d(sV + c * Ly::kChunk, &tmV, bar(KV_FULL), c * 64, k0, h, b);
       }
@@ -280,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(bar(QFULL0 + st), Ly::kTile);
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c)
+        for (int c = 0; c < LD / 64; ++c)
           ptx::tma_load_4d(sQ(st) + c * Ly::kChunk, &tmQ, bar(QFULL0 + st), c * 64, q0, h, b);
       } else {
         ptx::mbar_arrive(bar(QFULL0 + st));
@@ -294,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(bar(DOFULL0 + sd), Ly::kTile);
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c)
+        for (int c = 0; c < LD / 64; ++c)
           ptx::tma_load_4d(sdO(sd) + c * Ly::kChunk, &tmdO, bar(DOFULL0 + sd), c * 64, q0, h, b);
       }
       __syncwarp();
@@ -402,8 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool key_ok = kr < prm.N;
     const float sl2 = prm.scale * kLog2e;
     const int c0 = G * 32;                 // query columns [c0, c0 + 32) of S, dP
-    constexpr int kCols = HD / 4;          // this warp's dQ columns [G * kCols, +kCols)
+    // this warp's dQ columns [G * kCols, +kCols): d = 128, 64 all four
+    // column quarters; d = 96 (32) only the first three (two)
+    constexpr int kCols = LD / 4;
     constexpr int kUnits = kCols / 16;     // 2 KB units, contiguous in the accumulator
+    const bool dq_cols = HD == LD || G * kCols < HD;
     constexpr int kRedsHalf = kCols / 8;   // 16-byte reductions per lane per query block, halved
     // Vector reductions from registers queue in the SM sub-partition's memory
     // pipe ahead of the warp's own shared-memory loads, barrier waits and
@@ -415,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // vector reductions: at d = 128 in two halves, each right after the warp
     // has signalled its next dS and P results; at d = 64 (half the work per
     // block) right after the drain, while the warps wait for dV and dP.
-    constexpr bool kSplit = HD == 128;
-    const bool staged = qq <= 1;
+    constexpr bool kSplit = LD == 128;
+    const bool staged = qq <= 1 && dq_cols;
     constexpr bool det = kDet;             // store into this key block's slice instead of adding
     int rounds = 0;                        // bulk operations issued by this warp
     uint32_t pk[16];                       // P for columns c0 .. c0 + 31, bf16 pairs
@@ -444,13 +460,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto drain_dq = [&](int it) -> bool {
       if (!warp_wait(bar(DQ_FULL), it & 1, W)) return false;
       ptx::tc_fence_after();
-      if constexpr (kCols == 32) {
-        ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(dq));
-      } else {
-        ptx::tmem_ld16(tm + Ly::kColdQ + lane_off + G * 16, *reinterpret_cast<uint32_t(*)[16]>(dq));
+      if (dq_cols) {
+        if constexpr (kCols == 32) {
+          ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(dq));
+        } else {
+          ptx::tmem_ld16(tm + Ly::kColdQ + lane_off + G * 16, *reinterpret_cast<uint32_t(*)[16]>(dq));
+        }
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DQ_EMPTY));
+      if (!dq_cols) return true;
       dq_dst = prm.dq_accum + (det ? kb * prm.slice_elems : 0) +
                dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * kUnits, HD);
       if (staged) {
@@ -597,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD, bool kDet>
 cudaError_t launch_hd(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t s) {
-  using Ly = Layout<HD>;
+  using Ly = Layout<(HD <= 64 ? 64 : 128)>;
   cudaError_t e =
       cudaFuncSetAttribute(bwd_sm103_kernel<HD, kDet>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
@@ -665,8 +684,12 @@ cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, 
   prm.causal = p.causal;
   prm.slice_elems = deterministic(p) ? dq_slice_elems(p) : 0;
   const bool det = prm.slice_elems > 0;
-  if (p.d == 64) return det ? launch_hd<64, true>(p, maps, prm, s) : launch_hd<64, false>(p, maps, prm, s);
-  if (p.d == 128) return det ? launch_hd<128, true>(p, maps, prm, s) : launch_hd<128, false>(p, maps, prm, s);
+  switch (p.d) {
+    case 32: return det ? launch_hd<32, true>(p, maps, prm, s) : launch_hd<32, false>(p, maps, prm, s);
+    case 64: return det ? launch_hd<64, true>(p, maps, prm, s) : launch_hd<64, false>(p, maps, prm, s);
+    case 96: return det ? launch_hd<96, true>(p, maps, prm, s) : launch_hd<96, false>(p, maps, prm, s);
+    case 128: return det ? launch_hd<128, true>(p, maps, prm, s) : launch_hd<128, false>(p, maps, prm, s);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -1,4 +1,4 @@
-// Forward pass (companion of the backward) for bf16, head dim 64 or 128, on
+// Forward pass (companion of the backward) for bf16, head dim 32, 64, 96 or 128, on
 // the sm_100-family tensor cores.  Online softmax over 128-key blocks
 // (1point3acres FlashAttention write-up, online-softmax paragraphs; "CUDA
 // 算子工程" ch.16 §16.4 for L = m + log l):
@@ -76,10 +76,12 @@ enum BarId {
   kNumBars
 };
 
-template <int HD>
+// Tiles LD = 64 or 128 columns wide: head dims 32 and 64 use LD = 64, 96 and
+// 128 use LD = 128; the TMA zero-fills the columns past d.
+template <int LD>
 struct FwdLayout {
   static constexpr int kChunk = kBlk * 128;
-  static constexpr int kTile = kBlk * HD * 2;
+  static constexpr int kTile = kBlk * LD * 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTile;                 // kKStages tiles
   static constexpr int kV = kK + kKStages * kTile;      // kVStages tiles
@@ -89,7 +91,7 @@ struct FwdLayout {
   static constexpr int kBytes = kMisc + 16;
   static constexpr uint32_t kColO = kSBufs * 128;     // S/P buffers at 0, 128, 256
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kColO + HD <= kTmemCols, "tensor memory budget");
+  static_assert(kColO + LD <= kTmemCols, "tensor memory budget");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -117,7 +119,8 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const FwdParams prm) {
-  using Ly = FwdLayout<HD>;
+  constexpr int LD = HD <= 64 ? 64 : 128;
+  using Ly = FwdLayout<LD>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_addr(smem);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tmQ);
         ptx::mbar_arrive_expect_tx(bar(Q_FULL), Ly::kTile);
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) ptx::tma_load_4d(sQ + c * Ly::kChunk, &tmQ, bar(Q_FULL), c * 64, q0, h, b);
+        for (int c = 0; c < LD / 64; ++c) ptx::tma_load_4d(sQ + c * Ly::kChunk, &tmQ, bar(Q_FULL), c * 64, q0, h, b);
       }
     }
     for (int j = 0; j < n_blk; ++j) {
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dst = isK ? sK(st) : sV(st);
         ptx::mbar_arrive_expect_tx(bar(full0 + st), Ly::kTile);
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c)
+        for (int c = 0; c < LD / 64; ++c)
           ptx::tma_load_4d(dst + c * Ly::kChunk, map, bar(full0 + st), c * 64, j * kBlk, h, b);
       }
       __syncwarp();
@@ -324,18 +327,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(bar(O_DONE0 + (j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, W))) break;
         ptx::tc_fence_after();
         const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.f;
-        constexpr int kOC = HD / 2;
-        uint32_t o[kOC];
-        if constexpr (kOC == 64) {
-          ptx::tmem_ld64(tm + Ly::kColO + lane_off + G * 64, tm + Ly::kColO + lane_off + G * 64 + 32,
-                         *reinterpret_cast<uint32_t(*)[64]>(o));
-        } else {
-          ptx::tmem_ld32(tm + Ly::kColO + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(o));
+        constexpr int kOC = HD / 2;  // this warp's O columns, in 16-column pieces
+#pragma unroll
+        for (int c = 0; c < kOC; c += 16) {
+          uint32_t o[16];
+          ptx::tmem_ld16(tm + Ly::kColO + lane_off + G * kOC + c, o);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          ptx::tmem_st16(tm + Ly::kColO + lane_off + G * kOC + c, o);
         }
-#pragma unroll
-        for (int c = 0; c < kOC; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-#pragma unroll
-        for (int c = 0; c < kOC; c += 16) ptx::tmem_st16(tm + Ly::kColO + lane_off + G * kOC + c, &o[c]);
         ptx::tmem_st_wait();
         l_part *= alpha;
       }
@@ -365,21 +365,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float inv = 1.f / l;
         constexpr int kOC = HD / 2;
         __nv_bfloat16* orow = prm.O + head + (int64_t)qrow * prm.sn + G * kOC;
+        // 32-column pieces, then a 16-column tail (d = 32, 96)
+        auto put = [&](const uint32_t* o, int n, int c) {
 #pragma unroll
-        for (int c = 0; c < kOC; c += 32) {
+          for (int u = 0; u < n / 8; ++u) {
+            uint4 v;
+            v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+            v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+            v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+            v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c + 8 * u) = v;
+          }
+        };
+#pragma unroll
+        for (int c = 0; c + 32 <= kOC; c += 32) {
           uint32_t o[32];
           ptx::tmem_ld32(tm + Ly::kColO + lane_off + G * kOC + c, o);
-          if (qrow < prm.N) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint4 v;
-              v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
-              v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
-              v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
-              v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
-              *reinterpret_cast<uint4*>(orow + c + 8 * u) = v;
-            }
-          }
+          if (qrow < prm.N) put(o, 32, c);
+        }
+        if constexpr (kOC % 32 == 16) {
+          uint32_t o[16];
+          ptx::tmem_ld16(tm + Ly::kColO + lane_off + G * kOC + kOC - 16, o);
+          if (qrow < prm.N) put(o, 16, kOC - 16);
         }
         if (G == 0 && qrow < prm.N) prm.L[(int64_t)bh * prm.N + qrow] = (m_run + log2f(l)) * kLn2;
       }
@@ -396,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD>
 cudaError_t launch_fwd_hd(const fa_problem& p, const CUtensorMap* maps, const FwdParams& prm, cudaStream_t s) {
-  using Ly = FwdLayout<HD>;
+  using Ly = FwdLayout<(HD <= 64 ? 64 : 128)>;
   cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
@@ -426,8 +433,12 @@ cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, 
   prm.sn = p.stride_n;
   prm.scale = p.scale;
   prm.causal = p.causal;
-  if (p.d == 64) return launch_fwd_hd<64>(p, maps, prm, s);
-  if (p.d == 128) return launch_fwd_hd<128>(p, maps, prm, s);
+  switch (p.d) {
+    case 32: return launch_fwd_hd<32>(p, maps, prm, s);
+    case 64: return launch_fwd_hd<64>(p, maps, prm, s);
+    case 96: return launch_fwd_hd<96>(p, maps, prm, s);
+    case 128: return launch_fwd_hd<128>(p, maps, prm, s);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -27,9 +27,13 @@ uint64_t wait_limit_ns();
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 inline bool deterministic(const fa_problem& p) { return (p.flags & FA_FLAG_DETERMINISTIC) != 0; }
-// Key-block height of the backward kernel that serves p (tensor-core bf16
-// kernel: 128; CUDA-core fp32 kernel: 64).
-inline int key_block_rows(const fa_problem& p) { return p.dtype == FA_BF16 ? 128 : 64; }
+// bf16 with d <= 128 runs on the tensor-core kernels; fp32, and bf16 with
+// d = 256 (whose dK and dV accumulators alone would fill tensor memory), on
+// the CUDA-core kernels.
+inline bool tensor_core(const fa_problem& p) { return p.dtype == FA_BF16 && p.d <= 128; }
+// Key-block height of the backward kernel that serves p (tensor-core kernel:
+// 128; CUDA-core kernel: 64, or 32 at d = 256).
+inline int key_block_rows(const fa_problem& p) { return tensor_core(p) ? 128 : (p.d == 256 ? 32 : 64); }
 // dQ accumulator slices: one per key block in deterministic mode, else one.
 inline int64_t dq_slices(const fa_problem& p) {
   return deterministic(p) ? ceil_div(p.N, key_block_rows(p)) : 1;
@@ -43,18 +47,19 @@ inline int64_t dq_slice_elems(const fa_problem& p) {
 cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO, float* D,
                               float* dq_accum, cudaStream_t s);
 cudaError_t launch_convert_dq(const fa_problem& p, const float* dq_accum, void* dQ, cudaStream_t s);
-// CUDA-core forward for float32.
+// CUDA-core forward and backward (fp32, and bf16 at d = 256; fp32
+// arithmetic throughout).
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
                             void* O, float* L, cudaStream_t s);
-cudaError_t launch_bwd_simt_fp32(const fa_problem& p, const float* Q, const float* K, const float* V,
-                                 const float* dO, const float* L, const float* D, float* dq_accum,
-                                 float* dK, float* dV, cudaStream_t s);
-// tcgen05 / TMEM / TMA backward for bf16, d in {64, 128}.  Returns
+cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
+                            const void* dO, const float* L, const float* D, float* dq_accum,
+                            void* dK, void* dV, cudaStream_t s);
+// tcgen05 / TMEM / TMA backward for bf16, d in {32, 64, 96, 128}.  Returns
 // cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V,
                              const void* dO, const float* L, const float* D, float* dq_accum,
                              void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
-// tcgen05 forward for bf16, d in {64, 128}.
+// tcgen05 forward for bf16, d in {32, 64, 96, 128}.
 cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                              int32_t* status, uint64_t wait_ns, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t wait_ns, cudaStream_t s);

@@ -1,11 +1,14 @@
 // CUDA-core (FFMA) kernels for float32 problems (tensor cores have no fp32
 // mode that keeps float32 accuracy, and the fp32 workload is a small
-// correctness problem):
-//  * the forward pass (online softmax);
-//  * the backward pass.
-// Both use 64 x 64 tiles and 256 threads arranged 16 x 16; thread (ty, tx)
-// owns rows ty + 16a and columns tx + 16b of a tile, so the lanes that share
-// a row sit in one half-warp and reduce with 4 shuffles.
+// correctness problem) and for bf16 at d = 256 (whose dK and dV accumulators
+// alone would fill the tensor memory of the tcgen05 kernel); inputs are
+// widened to fp32 and all arithmetic is fp32:
+//  * the forward pass (online softmax), 64 x 64 tiles;
+//  * the backward pass, 64 x 64 tiles (32 x 32 at d = 256, to fit shared
+//    memory).
+// 256 threads arranged 16 x 16; thread (ty, tx) owns rows ty + 16a and
+// columns tx + 16b of a tile, so the lanes that share a row sit in one
+// half-warp and reduce with 4 shuffles.
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -25,13 +28,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void from_f(float* p, float v) { *p = v; }
+__device__ __forceinline__ void from_f(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
-// Copy a kT x HD tile of rows [row0, row0 + kT) into shared memory as fp32
+// Copy a ROWS x HD tile of rows [row0, row0 + ROWS) into shared memory as fp32
 // with row pitch `pitch`; rows >= N are zero.
-template <typename T, int HD>
+template <typename T, int HD, int ROWS = kT>
 __device__ __forceinline__ void load_tile(float* dst, int pitch, const T* src, int64_t sn, int row0, int N) {
-  for (int k = threadIdx.x; k < kT * HD; k += kThreads) {
+  for (int k = threadIdx.x; k < ROWS * HD; k += kThreads) {
     const int r = k / HD, c = k % HD;
     const int n = row0 + r;
     dst[r * pitch + c] = n < N ? to_f(src[(int64_t)n * sn + c]) : 0.f;
@@ -166,92 +171,93 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict_
 }
 
 // ----------------------------------------------------------------------------
-// fp32 backward.  One block per (b, h, 64-key block); inner loop over query
-// tiles.  dV and dK accumulate in registers; dQ partials go to the fp32
+// Backward.  One block per (b, h, KT-key block); inner loop over query tiles
+// of KT rows.  dV and dK accumulate in registers; dQ partials go to the fp32
 // accumulator with atomicAdd (unit-blocked layout of include/fa.h).
 // ----------------------------------------------------------------------------
-template <int HD>
-__global__ void __launch_bounds__(kThreads) bwd_simt_fp32_kernel(
-    const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
-    const float* __restrict__ dO, const float* __restrict__ Lg, const float* __restrict__ Dg,
-    float* __restrict__ dq_accum, float* __restrict__ dK, float* __restrict__ dV, int H, int N, int64_t sb,
-    int64_t sh, int64_t sn, float scale, int causal, int64_t slice_elems) {
+template <typename T, int HD, int KT>
+__global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
+    const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
+    const float* __restrict__ Lg, const float* __restrict__ Dg, float* __restrict__ dq_accum, T* __restrict__ dK,
+    T* __restrict__ dV, int H, int N, int64_t sb, int64_t sh, int64_t sn, float scale, int causal,
+    int64_t slice_elems) {
   // slice_elems > 0 (deterministic): this key block's dQ contributions are
   // stored into its own slice of the accumulator instead of added.
-  constexpr int kP = HD + 1, kPP = kT + 1;
+  constexpr int kP = HD + 1, kPP = KT + 1;
+  constexpr int kR = KT / 16;   // rows (and columns) of a tile per thread
   constexpr int kCols = HD / 16;
   extern __shared__ float smem[];
   float* sK = smem;
-  float* sV = sK + kT * kP;
-  float* sQ = sV + kT * kP;
-  float* sdO = sQ + kT * kP;
-  float* sP = sdO + kT * kP;   // [query][key]
-  float* sdS = sP + kT * kPP;  // [query][key]
-  float* sL = sdS + kT * kPP;  // L * log2(e), +inf for rows >= N
-  float* sD = sL + kT;
+  float* sV = sK + KT * kP;
+  float* sQ = sV + KT * kP;
+  float* sdO = sQ + KT * kP;
+  float* sP = sdO + KT * kP;   // [query][key]
+  float* sdS = sP + KT * kPP;  // [query][key]
+  float* sL = sdS + KT * kPP;  // L * log2(e), +inf for rows >= N
+  float* sD = sL + KT;
 
-  const int tiles = (N + kT - 1) / kT;
+  const int tiles = (N + KT - 1) / KT;
   const int kb = blockIdx.x % tiles;
   const int bh = blockIdx.x / tiles;
   const int b = bh / H, h = bh % H;
   const int64_t head = (int64_t)b * sb + (int64_t)h * sh;
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-  const int k0 = kb * kT;
+  const int k0 = kb * KT;
   const float sl2 = scale * kLog2e;
   const int acc_tiles = (N + kTileRows - 1) / kTileRows;
 
-  load_tile<float, HD>(sK, kP, K + head, sn, k0, N);
-  load_tile<float, HD>(sV, kP, V + head, sn, k0, N);
+  load_tile<T, HD, KT>(sK, kP, K + head, sn, k0, N);
+  load_tile<T, HD, KT>(sV, kP, V + head, sn, k0, N);
 
-  float dv[4][kCols], dk[4][kCols];
+  float dv[kR][kCols], dk[kR][kCols];
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int a = 0; a < kR; ++a)
 #pragma unroll
     for (int u = 0; u < kCols; ++u) dv[a][u] = dk[a][u] = 0.f;
 
   for (int qt = causal ? kb : 0; qt < tiles; ++qt) {
-    const int q0 = qt * kT;
+    const int q0 = qt * KT;
     __syncthreads();
-    load_tile<float, HD>(sQ, kP, Q + head, sn, q0, N);
-    load_tile<float, HD>(sdO, kP, dO + head, sn, q0, N);
-    if (threadIdx.x < kT) {
+    load_tile<T, HD, KT>(sQ, kP, Q + head, sn, q0, N);
+    load_tile<T, HD, KT>(sdO, kP, dO + head, sn, q0, N);
+    if (threadIdx.x < KT) {
       const int i = q0 + threadIdx.x;
       sL[threadIdx.x] = i < N ? Lg[(int64_t)bh * N + i] * kLog2e : INFINITY;
       sD[threadIdx.x] = i < N ? Dg[(int64_t)bh * N + i] : 0.f;
     }
     __syncthreads();
     // S, P and dP, dS for the (query a, key bb) entries this thread owns
-    float s[4][4], dp[4][4];
+    float s[kR][kR], dp[kR][kR];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < kR; ++a)
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) s[a][bb] = dp[a][bb] = 0.f;
+      for (int bb = 0; bb < kR; ++bb) s[a][bb] = dp[a][bb] = 0.f;
 #pragma unroll 2
     for (int c = 0; c < HD; ++c) {
-      float qv[4], gv[4], kv[4], vv[4];
+      float qv[kR], gv[kR], kv[kR], vv[kR];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
+      for (int a = 0; a < kR; ++a) {
         qv[a] = sQ[(ty + 16 * a) * kP + c];
         gv[a] = sdO[(ty + 16 * a) * kP + c];
       }
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
+      for (int bb = 0; bb < kR; ++bb) {
         kv[bb] = sK[(tx + 16 * bb) * kP + c];
         vv[bb] = sV[(tx + 16 * bb) * kP + c];
       }
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < kR; ++a)
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
+        for (int bb = 0; bb < kR; ++bb) {
           s[a][bb] = fmaf(qv[a], kv[bb], s[a][bb]);
           dp[a][bb] = fmaf(gv[a], vv[bb], dp[a][bb]);
         }
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int a = 0; a < kR; ++a) {
       const int il = ty + 16 * a, i = q0 + il;
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
+      for (int bb = 0; bb < kR; ++bb) {
         const int jl = tx + 16 * bb, j = k0 + jl;
         const bool masked = (j >= N) || (causal && j > i);
         const float p = masked ? 0.f : ptx::ex2(fmaf(s[a][bb], sl2, -sL[il]));
@@ -262,10 +268,10 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_fp32_kernel(
     __syncthreads();
     // dV[j] += sum_i P[i][j] dO[i];  dK[j] += sum_i dS[i][j] Q[i]
 #pragma unroll 2
-    for (int i = 0; i < kT; ++i) {
-      float pv[4], sv[4];
+    for (int i = 0; i < KT; ++i) {
+      float pv[kR], sv[kR];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
+      for (int a = 0; a < kR; ++a) {
         pv[a] = sP[i * kPP + ty + 16 * a];
         sv[a] = sdS[i * kPP + ty + 16 * a];
       }
@@ -274,32 +280,32 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_fp32_kernel(
         const float g = sdO[i * kP + tx + 16 * u];
         const float q = sQ[i * kP + tx + 16 * u];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < kR; ++a) {
           dv[a][u] = fmaf(pv[a], g, dv[a][u]);
           dk[a][u] = fmaf(sv[a], q, dk[a][u]);
         }
       }
     }
     // dQ[i] partial = sum_j dS[i][j] K[j]
-    float dq[4][kCols];
+    float dq[kR][kCols];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int a = 0; a < kR; ++a)
 #pragma unroll
       for (int u = 0; u < kCols; ++u) dq[a][u] = 0.f;
 #pragma unroll 2
-    for (int j = 0; j < kT; ++j) {
-      float sv[4];
+    for (int j = 0; j < KT; ++j) {
+      float sv[kR];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) sv[a] = sdS[(ty + 16 * a) * kPP + j];
+      for (int a = 0; a < kR; ++a) sv[a] = sdS[(ty + 16 * a) * kPP + j];
 #pragma unroll
       for (int u = 0; u < kCols; ++u) {
         const float kv = sK[j * kP + tx + 16 * u];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) dq[a][u] = fmaf(sv[a], kv, dq[a][u]);
+        for (int a = 0; a < kR; ++a) dq[a][u] = fmaf(sv[a], kv, dq[a][u]);
       }
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int a = 0; a < kR; ++a) {
       const int i = q0 + ty + 16 * a;
       if (i >= N) continue;
 #pragma unroll
@@ -313,14 +319,14 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_fp32_kernel(
     }
   }
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
+  for (int a = 0; a < kR; ++a) {
     const int j = k0 + ty + 16 * a;
     if (j >= N) continue;
 #pragma unroll
     for (int u = 0; u < kCols; ++u) {
       const int c = tx + 16 * u;
-      dV[head + (int64_t)j * sn + c] = dv[a][u];
-      dK[head + (int64_t)j * sn + c] = scale * dk[a][u];
+      from_f(dV + head + (int64_t)j * sn + c, dv[a][u]);
+      from_f(dK + head + (int64_t)j * sn + c, scale * dk[a][u]);
     }
   }
 }
@@ -354,42 +360,61 @@ cudaError_t launch_fwd_dt(const fa_problem& p, const void* Q, const void* K, con
     case 16: return launch_fwd_t<T, 16>(p, q, k, v, o, L, s);
     case 32: return launch_fwd_t<T, 32>(p, q, k, v, o, L, s);
     case 64: return launch_fwd_t<T, 64>(p, q, k, v, o, L, s);
+    case 96: return launch_fwd_t<T, 96>(p, q, k, v, o, L, s);
     case 128: return launch_fwd_t<T, 128>(p, q, k, v, o, L, s);
+    case 256: return launch_fwd_t<T, 256>(p, q, k, v, o, L, s);
   }
   return cudaErrorInvalidValue;
 }
 
-template <int HD>
-cudaError_t launch_bwd_fp32_t(const fa_problem& p, const float* Q, const float* K, const float* V, const float* dO,
-                              const float* L, const float* D, float* acc, float* dK, float* dV, cudaStream_t s) {
-  const size_t sm = sizeof(float) * (size_t)(4 * kT * (HD + 1) + 2 * kT * (kT + 1) + 2 * kT);
-  cudaError_t e = set_smem(bwd_simt_fp32_kernel<HD>, sm);
+template <typename T, int HD>
+cudaError_t launch_bwd_t(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
+                         const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s) {
+  constexpr int KT = HD == 256 ? 32 : kT;
+  const size_t sm = sizeof(float) * (size_t)(4 * KT * (HD + 1) + 2 * KT * (KT + 1) + 2 * KT);
+  cudaError_t e = set_smem(bwd_simt_kernel<T, HD, KT>, sm);
   if (e != cudaSuccess) return e;
-  const int tiles = (p.N + kT - 1) / kT;
+  const int tiles = (p.N + KT - 1) / KT;
   const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
-  bwd_simt_fp32_kernel<HD><<<grid, kThreads, sm, s>>>(Q, K, V, dO, L, D, acc, dK, dV, p.H, p.N, p.stride_b,
-                                                      p.stride_h, p.stride_n, p.scale, p.causal,
-                                                      deterministic(p) ? dq_slice_elems(p) : 0);
+  bwd_simt_kernel<T, HD, KT><<<grid, kThreads, sm, s>>>(
+      (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, L, D, acc, (T*)dK, (T*)dV, p.H, p.N, p.stride_b,
+      p.stride_h, p.stride_n, p.scale, p.causal, deterministic(p) ? dq_slice_elems(p) : 0);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_bwd_dt(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
+                          const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s) {
+  switch (p.d) {
+    case 16: return launch_bwd_t<T, 16>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
+    case 32: return launch_bwd_t<T, 32>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
+    case 64: return launch_bwd_t<T, 64>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
+    case 96: return launch_bwd_t<T, 96>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
+    case 128: return launch_bwd_t<T, 128>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
+    case 256: return launch_bwd_t<T, 256>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
+// fp32 at every supported d; bf16 only at d = 256 (the tensor-core kernels
+// serve the other bf16 head dims), so only that bf16 instance is built.
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                             cudaStream_t s) {
+  if (p.dtype == FA_BF16)
+    return p.d == 256 ? launch_fwd_t<__nv_bfloat16, 256>(p, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K,
+                                                         (const __nv_bfloat16*)V, (__nv_bfloat16*)O, L, s)
+                      : cudaErrorInvalidValue;
   return launch_fwd_dt<float>(p, Q, K, V, O, L, s);
 }
 
-cudaError_t launch_bwd_simt_fp32(const fa_problem& p, const float* Q, const float* K, const float* V,
-                                 const float* dO, const float* L, const float* D, float* acc, float* dK, float* dV,
-                                 cudaStream_t s) {
-  switch (p.d) {
-    case 16: return launch_bwd_fp32_t<16>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-    case 32: return launch_bwd_fp32_t<32>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-    case 64: return launch_bwd_fp32_t<64>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-    case 128: return launch_bwd_fp32_t<128>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-  }
-  return cudaErrorInvalidValue;
+cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
+                            const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s) {
+  if (p.dtype == FA_BF16)
+    return p.d == 256 ? launch_bwd_t<__nv_bfloat16, 256>(p, Q, K, V, dO, L, D, acc, dK, dV, s)
+                      : cudaErrorInvalidValue;
+  return launch_bwd_dt<float>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
 }
 
 }  // namespace fa

@@ -41,9 +41,12 @@
  *    reach the accumulator in whatever order the hardware completes its
  *    reductions (the FA2 default; ch.16 §16.3 notes deterministic=False).
  *
- * Supported problems: dtype FA_BF16 with d in {64, 128} (tcgen05 tensor-core
- * kernels), dtype FA_FP32 with d in {16, 32, 64, 128} (exact fp32 FFMA
+ * Supported problems: dtype FA_BF16 with d in {32, 64, 96, 128} (tcgen05
+ * tensor-core kernels) or d = 256 (CUDA-core kernels with fp32 arithmetic:
+ * at d = 256 the dK and dV accumulators alone would fill tensor memory);
+ * dtype FA_FP32 with d in {16, 32, 64, 96, 128, 256} (exact fp32 FFMA
  * kernels, no TF32).  N >= 1, B >= 1, H >= 1, N <= 2^24, B*H <= 2^24.
+ * Other d return FA_ERR_UNSUPPORTED.
  *
  * dQ accumulator layout
  * ---------------------
@@ -104,8 +107,9 @@ typedef struct {
 
 /* Number of float32 elements of the dQ accumulator for problem p, or 0 if p
  * is NULL or invalid: B * H * ceil(N/128) * 128 * d, times the number of key
- * blocks (ceil(N/128) for bf16, ceil(N/64) for fp32) with
- * FA_FLAG_DETERMINISTIC. */
+ * blocks with FA_FLAG_DETERMINISTIC: ceil(N/128) on the tensor-core kernels
+ * (bf16, d <= 128), ceil(N/64) on the CUDA-core kernels, ceil(N/32) on those
+ * at d = 256. */
 size_t fa_dq_accum_elems(const fa_problem* p);
 
 /* Forward pass, companion of the backward: O = softmax(scale Q K^T) V and

@@ -52,14 +52,21 @@ def test_dq_accum_size(lib):
     assert fa.fa_dq_accum_elems(p) == 4 * 16 * 32 * 128 * 128
     p = _prob(N=48, d=16, H=1, dtype=fa.FA_FP32, stride_b=48 * 16, stride_h=48 * 16, stride_n=16)
     assert fa.fa_dq_accum_elems(p) == 128 * 16
-    assert fa.fa_dq_accum_elems(_prob(d=96, stride_n=96)) == 0
-    # deterministic: one slice per key block (128 keys for bf16, 64 for fp32)
+    assert fa.fa_dq_accum_elems(_prob(d=96, stride_n=96)) == 1 * 2 * 128 * 96
+    assert fa.fa_dq_accum_elems(_prob(d=48, stride_n=48)) == 0  # unsupported head dim
+    # deterministic: one slice per key block (128 keys on the tensor-core
+    # kernels, 64 on the CUDA-core kernels, 32 on those at d = 256)
     p = _prob(N=4000, d=128, H=16, B=4, stride_b=16 * 4000 * 128, stride_h=4000 * 128, stride_n=128,
               flags=fa.FA_FLAG_DETERMINISTIC)
     assert fa.fa_dq_accum_elems(p) == 32 * 4 * 16 * 32 * 128 * 128
     p = _prob(N=48, d=16, H=1, dtype=fa.FA_FP32, stride_b=48 * 16, stride_h=48 * 16, stride_n=16,
               flags=fa.FA_FLAG_DETERMINISTIC)
     assert fa.fa_dq_accum_elems(p) == 1 * 128 * 16
+    p = _prob(N=100, d=256, H=1, stride_b=100 * 256, stride_h=100 * 256, stride_n=256,
+              flags=fa.FA_FLAG_DETERMINISTIC)
+    assert fa.fa_dq_accum_elems(p) == 4 * 128 * 256
+    p = _prob(N=100, d=96, H=1, stride_b=100 * 96, stride_h=100 * 96, stride_n=96, flags=fa.FA_FLAG_DETERMINISTIC)
+    assert fa.fa_dq_accum_elems(p) == 1 * 128 * 96
 
 
 BAD = 0x1000  # a 16-byte aligned dummy address; validation fails before any use
@@ -70,8 +77,10 @@ BAD = 0x1000  # a 16-byte aligned dummy address; validation fails before any use
     [
         (dict(N=0), fa.FA_ERR_INVALID_ARG),
         (dict(B=0), fa.FA_ERR_INVALID_ARG),
-        (dict(d=96, stride_n=96), fa.FA_ERR_UNSUPPORTED),
-        (dict(d=32), fa.FA_ERR_UNSUPPORTED),  # bf16 path: d in {64, 128}
+        (dict(d=48, stride_n=48), fa.FA_ERR_UNSUPPORTED),  # d in {32, 64, 96, 128, 256} for bf16
+        (dict(d=16, stride_n=16), fa.FA_ERR_UNSUPPORTED),
+        (dict(d=512, stride_n=512), fa.FA_ERR_UNSUPPORTED),
+        (dict(d=80, stride_n=80, dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),
         (dict(causal=2), fa.FA_ERR_INVALID_ARG),
         (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
         (dict(flags=2), fa.FA_ERR_INVALID_ARG),

@@ -31,7 +31,10 @@ def _accum_index(B, H, N, d):
 
 
 @pytest.mark.parametrize("dtype,d,N", [(torch.bfloat16, 64, 300), (torch.bfloat16, 128, 129),
-                                       (torch.float32, 16, 48), (torch.float32, 128, 1)])
+                                       (torch.float32, 16, 48), (torch.float32, 128, 1),
+                                       (torch.bfloat16, 96, 200), (torch.bfloat16, 32, 130),
+                                       (torch.bfloat16, 256, 129), (torch.float32, 96, 77),
+                                       (torch.float32, 256, 300)])
 def test_preprocess_computes_D_and_zeroes_accumulator(dtype, d, N):
     B, H = 2, 3
     gen = torch.Generator().manual_seed(5)
@@ -48,7 +51,9 @@ def test_preprocess_computes_D_and_zeroes_accumulator(dtype, d, N):
 
 
 @pytest.mark.parametrize("dtype,d,N", [(torch.bfloat16, 128, 300), (torch.bfloat16, 64, 128),
-                                       (torch.float32, 16, 48), (torch.float32, 32, 257)])
+                                       (torch.float32, 16, 48), (torch.float32, 32, 257),
+                                       (torch.bfloat16, 96, 129), (torch.bfloat16, 256, 200),
+                                       (torch.float32, 96, 130), (torch.float32, 256, 1)])
 def test_convert_undoes_the_documented_layout(dtype, d, N):
     B, H = 2, 2
     q = torch.empty(B, H, N, d, dtype=dtype)
