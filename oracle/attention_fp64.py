@@ -25,9 +25,14 @@ online softmax, so a reader can check it against the pages by eye:
 
 Readings where the pages leave a step open:
 
-* causal masking is top-left aligned with N_q == N_k: key j is visible to
+* causal masking: the pages show only N_q == N_k, where key j is visible to
   query i iff j <= i (CS349E lecture 11 demo 4 masks the upper triangle;
-  masked scores are -inf so their P is exactly 0);
+  masked scores are -inf so their P is exactly 0).  For N_q != N_k the mask
+  is aligned bottom-right, j <= i + (N_k - N_q): the last query sees every
+  key, and at N_q == N_k this is the pages' mask;
+* a query row that sees no key at all (causal, N_q > N_k) has an empty
+  softmax: its O row is 0, its L is +inf (so that exp(S - L) = 0 in the
+  backward) and its gradients are 0;
 * D is computed by its definition (row sum of P * dP); the identity
   D_i = dO_i . O_i (ch.16 §16.1) is returned separately as ``D_from_O`` so
   tests can check the identity rather than assume it;
@@ -61,15 +66,15 @@ __all__ = [
 
 @dataclass
 class AttentionGrads:
-    """All float64 results for one (B, H, N, d) problem."""
+    """All float64 results for one (B, H, N_q, N_k, d) problem."""
 
-    O: np.ndarray  # [B, H, N, d]
-    L: np.ndarray  # [B, H, N]
-    D: np.ndarray  # [B, H, N]   row sums of P * dP (definition)
-    D_from_O: np.ndarray  # [B, H, N]  dO_i . O_i (identity of ch.16 §16.1)
-    dQ: np.ndarray  # [B, H, N, d]
-    dK: np.ndarray  # [B, H, N, d]
-    dV: np.ndarray  # [B, H, N, d]
+    O: np.ndarray  # [B, H, N_q, d]
+    L: np.ndarray  # [B, H, N_q]
+    D: np.ndarray  # [B, H, N_q]   row sums of P * dP (definition)
+    D_from_O: np.ndarray  # [B, H, N_q]  dO_i . O_i (identity of ch.16 §16.1)
+    dQ: np.ndarray  # [B, H, N_q, d]
+    dK: np.ndarray  # [B, H, N_k, d]
+    dV: np.ndarray  # [B, H, N_k, d]
 
 
 def _as4d(x: np.ndarray) -> np.ndarray:
@@ -81,14 +86,15 @@ def _as4d(x: np.ndarray) -> np.ndarray:
     return x
 
 
-def _scores(q_rows: np.ndarray, k: np.ndarray, scale: float, row0: int, causal: bool) -> np.ndarray:
+def _scores(q_rows: np.ndarray, k: np.ndarray, scale: float, row0: int, causal: bool, offset: int) -> np.ndarray:
     """S for a block of query rows starting at global row ``row0``: scale * Q K^T,
-    with -inf where key j > query i under the causal mask."""
+    with -inf where key j > query i + offset under the causal mask
+    (offset = N_k - N_q)."""
     s = scale * (q_rows @ k.T)
     if causal:
         i = np.arange(row0, row0 + q_rows.shape[0])[:, None]
         j = np.arange(k.shape[0])[None, :]
-        s = np.where(j > i, -np.inf, s)
+        s = np.where(j > i + offset, -np.inf, s)
     return s
 
 
@@ -96,27 +102,33 @@ def _softmax_rows(s: np.ndarray):
     """Row-wise max m, logsumexp L = m + log(sum exp(S - m)) and P = exp(S - L).
 
     Masked entries (-inf) give exactly 0.  The max is subtracted before the
-    exponential as in the write-up's safe-softmax statistics (m, l)."""
+    exponential as in the write-up's safe-softmax statistics (m, l).  A row
+    with every entry masked gets L = +inf and P = 0."""
     m = np.max(s, axis=1)
-    ell = np.sum(np.exp(s - m[:, None]), axis=1)
-    L = m + np.log(ell)
-    P = np.exp(s - L[:, None])
+    empty = m == -np.inf
+    m_safe = np.where(empty, 0.0, m)
+    ell = np.sum(np.exp(s - m_safe[:, None]), axis=1)
+    with np.errstate(divide="ignore"):
+        L = np.where(empty, np.inf, m_safe + np.log(np.where(empty, 1.0, ell)))
+    P = np.where(empty[:, None], 0.0, np.exp(s - np.where(empty, 0.0, L)[:, None]))
     return L, P
 
 
 def attention_forward(Q, K, V, scale: float, causal: bool = False, rows: int = 512):
     """Dense forward: returns (O, L), both float64.
 
-    Q, K, V: [N, d] or [B, H, N, d].  ``rows`` only bounds memory."""
+    Q: [N_q, d] or [B, H, N_q, d]; K, V: [N_k, d] or [B, H, N_k, d].
+    ``rows`` only bounds memory."""
     Q, K, V = _as4d(Q), _as4d(K), _as4d(V)
     B, H, N, d = Q.shape
+    offset = K.shape[2] - N
     O = np.empty((B, H, N, V.shape[-1]))
     L = np.empty((B, H, N))
     for b in range(B):
         for h in range(H):
             for r0 in range(0, N, rows):
                 r1 = min(N, r0 + rows)
-                s = _scores(Q[b, h, r0:r1], K[b, h], scale, r0, causal)
+                s = _scores(Q[b, h, r0:r1], K[b, h], scale, r0, causal, offset)
                 Lr, P = _softmax_rows(s)
                 L[b, h, r0:r1] = Lr
                 O[b, h, r0:r1] = P @ V[b, h]
@@ -131,20 +143,22 @@ def attention_backward(Q, K, V, dO, scale: float, causal: bool = False, rows: in
     dK = scale dS^T Q.  Returns float64 O, L, D, D_from_O, dQ, dK, dV."""
     Q, K, V, dO = _as4d(Q), _as4d(K), _as4d(V), _as4d(dO)
     B, H, N, d = Q.shape
+    Nk = K.shape[2]
+    offset = Nk - N
     dv_dim = V.shape[-1]
     O = np.empty((B, H, N, dv_dim))
     L = np.empty((B, H, N))
     D = np.empty((B, H, N))
     D_from_O = np.empty((B, H, N))
     dQ = np.empty((B, H, N, d))
-    dK = np.zeros((B, H, N, d))
-    dV = np.zeros((B, H, N, dv_dim))
+    dK = np.zeros((B, H, Nk, d))
+    dV = np.zeros((B, H, Nk, dv_dim))
     for b in range(B):
         for h in range(H):
             q, k, v, g = Q[b, h], K[b, h], V[b, h], dO[b, h]
             for r0 in range(0, N, rows):
                 r1 = min(N, r0 + rows)
-                s = _scores(q[r0:r1], k, scale, r0, causal)          # S (rows x N)
+                s = _scores(q[r0:r1], k, scale, r0, causal, offset)  # S (rows x N_k)
                 Lr, P = _softmax_rows(s)                              # L, P
                 o = P @ v                                             # O = P V
                 dV[b, h] += P.T @ g[r0:r1]                            # dV = P^T dO
@@ -162,77 +176,82 @@ def attention_backward(Q, K, V, dO, scale: float, causal: bool = False, rows: in
 
 def attention_backward_loops(Q, K, V, dO, scale: float, causal: bool = False) -> AttentionGrads:
     """The same backward with explicit Python loops and no BLAS, for tiny
-    [N, d] inputs only (seconds at N=48, d=16).  Every sum is written as a
-    loop over its index, in the order of ch.16 §16.1."""
+    [N_q, d] x [N_k, d] inputs only (seconds at N = 48, d = 16).  Every sum is
+    written as a loop over its index, in the order of ch.16 §16.1."""
     q = np.asarray(Q, dtype=np.float64)
     k = np.asarray(K, dtype=np.float64)
     v = np.asarray(V, dtype=np.float64)
     g = np.asarray(dO, dtype=np.float64)
-    N, d = q.shape
+    nq, d = q.shape
+    nk = k.shape[0]
+    offset = nk - nq
     dv_dim = v.shape[1]
-    S = [[0.0] * N for _ in range(N)]
-    for i in range(N):
-        for j in range(N):
-            if causal and j > i:
+    S = [[0.0] * nk for _ in range(nq)]
+    for i in range(nq):
+        for j in range(nk):
+            if causal and j > i + offset:
                 S[i][j] = -math.inf
             else:
                 acc = 0.0
                 for c in range(d):
                     acc += q[i, c] * k[j, c]
                 S[i][j] = scale * acc
-    P = [[0.0] * N for _ in range(N)]
-    L = [0.0] * N
-    for i in range(N):
+    P = [[0.0] * nk for _ in range(nq)]
+    L = [0.0] * nq
+    for i in range(nq):
         m = max(S[i])
+        if m == -math.inf:  # no visible key: empty softmax
+            L[i] = math.inf
+            continue
         ell = 0.0
-        for j in range(N):
+        for j in range(nk):
             ell += math.exp(S[i][j] - m) if S[i][j] != -math.inf else 0.0
         L[i] = m + math.log(ell)
-        for j in range(N):
+        for j in range(nk):
             P[i][j] = math.exp(S[i][j] - L[i]) if S[i][j] != -math.inf else 0.0
-    O = np.zeros((N, dv_dim))
-    for i in range(N):
+    O = np.zeros((nq, dv_dim))
+    for i in range(nq):
         for c in range(dv_dim):
             acc = 0.0
-            for j in range(N):
+            for j in range(nk):
                 acc += P[i][j] * v[j, c]
             O[i, c] = acc
-    dV = np.zeros((N, dv_dim))
-    for j in range(N):
+    dV = np.zeros((nk, dv_dim))
+    for j in range(nk):
         for c in range(dv_dim):
             acc = 0.0
-            for i in range(N):
+            for i in range(nq):
                 acc += P[i][j] * g[i, c]
             dV[j, c] = acc
-    dP = [[0.0] * N for _ in range(N)]
-    for i in range(N):
-        for j in range(N):
+    dP = [[0.0] * nk for _ in range(nq)]
+    for i in range(nq):
+        for j in range(nk):
             acc = 0.0
             for c in range(dv_dim):
                 acc += g[i, c] * v[j, c]
             dP[i][j] = acc
-    D = [0.0] * N
-    for i in range(N):
+    D = [0.0] * nq
+    for i in range(nq):
         acc = 0.0
-        for j in range(N):
+        for j in range(nk):
             acc += P[i][j] * dP[i][j]
         D[i] = acc
-    dS = [[P[i][j] * (dP[i][j] - D[i]) for j in range(N)] for i in range(N)]
-    dQ = np.zeros((N, d))
-    dK = np.zeros((N, d))
-    for i in range(N):
+    dS = [[P[i][j] * (dP[i][j] - D[i]) for j in range(nk)] for i in range(nq)]
+    dQ = np.zeros((nq, d))
+    dK = np.zeros((nk, d))
+    for i in range(nq):
         for c in range(d):
             acc = 0.0
-            for j in range(N):
+            for j in range(nk):
                 acc += dS[i][j] * k[j, c]
             dQ[i, c] = scale * acc
-    for j in range(N):
+    for j in range(nk):
         for c in range(d):
             acc = 0.0
-            for i in range(N):
+            for i in range(nq):
                 acc += dS[i][j] * q[i, c]
             dK[j, c] = scale * acc
-    D_from_O = np.array([sum(g[i, c] * O[i, c] for c in range(dv_dim)) for i in range(N)])
+    D_from_O = np.array([sum(g[i, c] * O[i, c] for c in range(dv_dim)) for i in range(nq)])
     return AttentionGrads(O=O[None, None], L=np.array(L)[None, None], D=np.array(D)[None, None],
                           D_from_O=D_from_O[None, None], dQ=dQ[None, None], dK=dK[None, None],
                           dV=dV[None, None])
