@@ -70,6 +70,11 @@ class FaProblem(ctypes.Structure):
         ("stride_b", ctypes.c_int64),
         ("stride_h", ctypes.c_int64),
         ("stride_n", ctypes.c_int64),
+        ("N_k", ctypes.c_int32),  # 0: N_k = N, K-shaped strides = Q strides
+        ("reserved", ctypes.c_int32),
+        ("kstride_b", ctypes.c_int64),
+        ("kstride_h", ctypes.c_int64),
+        ("kstride_n", ctypes.c_int64),
     ]
 
 
@@ -138,26 +143,54 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def problem_for(q: torch.Tensor, scale: float, causal: bool, deterministic: bool = False) -> FaProblem:
-    """Problem descriptor for [B, H, N, d] tensors laid out like ``q``."""
+def problem_for(q: torch.Tensor, scale: float, causal: bool, deterministic: bool = False,
+                k: Optional[torch.Tensor] = None) -> FaProblem:
+    """Problem descriptor for Q-shaped [B, H, N, d] tensors laid out like ``q``
+    and, if ``k`` is given, K-shaped [B, H, N_k, d] tensors laid out like ``k``
+    (otherwise N_k = N with q's strides).  Causal masks are aligned
+    bottom-right: key j is visible to query i iff j <= i + N_k - N."""
     if q.dim() != 4:
         raise ValueError("expected a [B, H, N, d] tensor")
     if q.stride(3) != 1:
         raise ValueError("the last dimension must be contiguous")
     B, H, N, d = q.shape
     flags = FA_FLAG_DETERMINISTIC if deterministic else 0
-    return FaProblem(B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), flags,
-                     q.stride(0), q.stride(1), q.stride(2))
+    p = FaProblem(B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), flags,
+                  q.stride(0), q.stride(1), q.stride(2))
+    if k is not None:
+        if k.dim() != 4 or k.shape[0] != B or k.shape[1] != H or k.shape[3] != d or k.stride(3) != 1:
+            raise ValueError("k must be a [B, H, N_k, d] tensor with a contiguous last dimension")
+        p.N_k = k.shape[2]
+        p.kstride_b, p.kstride_h, p.kstride_n = k.stride(0), k.stride(1), k.stride(2)
+    return p
+
+
+def _k_rows(p: FaProblem):
+    """Rows and strides of the K-shaped tensors of p."""
+    if p.N_k == 0:
+        return p.N, (p.stride_b, p.stride_h, p.stride_n, 1)
+    return p.N_k, (p.kstride_b, p.kstride_h, p.kstride_n, 1)
+
+
+def _check_tensors(p: FaProblem, shape, strides, ts) -> None:
+    for t in ts:
+        if tuple(t.shape) != shape or t.stride() != strides:
+            raise ValueError(f"tensor of shape {tuple(t.shape)} strides {t.stride()}: expected {shape} {strides}")
+        if _dtype_code(t) != p.dtype:
+            raise ValueError("all [B, H, rows, d] tensors must share the dtype")
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
 
 
 def _same_layout(p: FaProblem, *ts: torch.Tensor) -> None:
-    for t in ts:
-        if t.shape != (p.B, p.H, p.N, p.d) or t.stride() != (p.stride_b, p.stride_h, p.stride_n, 1):
-            raise ValueError("all [B, H, N, d] tensors must share shape and strides")
-        if _dtype_code(t) != p.dtype:
-            raise ValueError("all [B, H, N, d] tensors must share the dtype")
-        if not t.is_cuda:
-            raise ValueError("tensors must be on a CUDA device")
+    """Q-shaped tensors: [B, H, N, d] with the Q strides."""
+    _check_tensors(p, (p.B, p.H, p.N, p.d), (p.stride_b, p.stride_h, p.stride_n, 1), ts)
+
+
+def _k_layout(p: FaProblem, *ts: torch.Tensor) -> None:
+    """K-shaped tensors: [B, H, N_k, d] with the K strides."""
+    rows, strides = _k_rows(p)
+    _check_tensors(p, (p.B, p.H, rows, p.d), strides, ts)
 
 
 def _rows(p: FaProblem, *ts: torch.Tensor) -> None:
@@ -181,7 +214,8 @@ def fa_dq_accum_elems(p: FaProblem) -> int:
 
 
 def fa_fwd(p: FaProblem, q, k, v, o, L, stream=None) -> None:
-    _same_layout(p, q, k, v, o)
+    _same_layout(p, q, o)
+    _k_layout(p, k, v)
     _rows(p, L)
     _check(load_library().fa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(L), _stream(stream)),
            "fa_fwd")
@@ -201,7 +235,8 @@ def _accum(p: FaProblem, acc: torch.Tensor) -> None:
 
 
 def fa_bwd(p: FaProblem, q, k, v, do, L, D, dq_accum, dk, dv, stream=None) -> None:
-    _same_layout(p, q, k, v, do, dk, dv)
+    _same_layout(p, q, do)
+    _k_layout(p, k, v, dk, dv)
     _rows(p, L, D)
     _accum(p, dq_accum)
     _check(load_library().fa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(L), _ptr(D),
@@ -216,7 +251,8 @@ def fa_convert_dq(p: FaProblem, dq_accum, dq, stream=None) -> None:
 
 
 def fa_backward(p: FaProblem, q, k, v, o, do, L, D, dq_accum, dq, dk, dv, stream=None) -> None:
-    _same_layout(p, q, k, v, o, do, dq, dk, dv)
+    _same_layout(p, q, o, do, dq)
+    _k_layout(p, k, v, dk, dv)
     _rows(p, L, D)
     _accum(p, dq_accum)
     _check(load_library().fa_backward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(L),
@@ -225,8 +261,9 @@ def fa_backward(p: FaProblem, q, k, v, o, do, L, D, dq_accum, dq, dk, dv, stream
 
 
 def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
-    """O, L for contiguous [B, H, N, d] CUDA tensors (bf16 or fp32)."""
-    p = problem_for(q, scale, causal)
+    """O, L for [B, H, N, d] queries and [B, H, N_k, d] keys/values (CUDA, bf16
+    or fp32; last dimension contiguous)."""
+    p = problem_for(q, scale, causal, k=k)
     o = torch.empty_like(q)
     L = torch.empty((p.B, p.H, p.N), dtype=torch.float32, device=q.device)
     fa_fwd(p, q, k, v, o, L, stream)
@@ -236,7 +273,7 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
 def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, stream=None, workspace=None,
                        deterministic: bool = False):
     """dQ, dK, dV.  ``workspace`` may pass preallocated (D, dq_accum)."""
-    p = problem_for(q, scale, causal, deterministic)
+    p = problem_for(q, scale, causal, deterministic, k=k)
     if workspace is None:
         D = torch.empty((p.B, p.H, p.N), dtype=torch.float32, device=q.device)
         acc = torch.empty(fa_dq_accum_elems(p), dtype=torch.float32, device=q.device)
@@ -255,9 +292,10 @@ def fa_backward_host(p: FaProblem, q, k, v, o, do, L, dq, dk, dv, workspace, hea
                      stream=None) -> None:
     """Backward from host tensors (dense, ideally pinned) through a device
     workspace; see include/fa.h."""
-    for t in (q, k, v, o, do, dq, dk, dv):
-        if t.is_cuda or not t.is_contiguous() or t.shape != (p.B, p.H, p.N, p.d) or _dtype_code(t) != p.dtype:
-            raise ValueError("host tensors must be dense [B, H, N, d] CPU tensors of the problem dtype")
+    rows_k, _ = _k_rows(p)
+    for t, rows in ((q, p.N), (o, p.N), (do, p.N), (dq, p.N), (k, rows_k), (v, rows_k), (dk, rows_k), (dv, rows_k)):
+        if t.is_cuda or not t.is_contiguous() or t.shape != (p.B, p.H, rows, p.d) or _dtype_code(t) != p.dtype:
+            raise ValueError("host tensors must be dense [B, H, rows, d] CPU tensors of the problem dtype")
     if L.is_cuda or not L.is_contiguous() or L.numel() != p.B * p.H * p.N or L.dtype != torch.float32:
         raise ValueError("L must be a dense float32 CPU tensor of B*H*N elements")
     if not workspace.is_cuda:
@@ -271,12 +309,12 @@ def fa_backward_host(p: FaProblem, q, k, v, o, do, L, dq, dk, dv, workspace, hea
 def attention_backward_host(q, k, v, o, do, L, scale: float, causal: bool = False, heads_per_group: int = 0,
                             workspace=None, out=None, stream=None, deterministic: bool = False):
     """dQ, dK, dV (pinned host tensors) for host-resident inputs."""
-    p = problem_for(q, scale, causal, deterministic)
+    p = problem_for(q, scale, causal, deterministic, k=k)
     if workspace is None:
         workspace = torch.empty(fa_backward_host_workspace_bytes(p, heads_per_group), dtype=torch.uint8,
                                 device="cuda")
     if out is None:
-        out = tuple(torch.empty_like(q).pin_memory() for _ in range(3))
+        out = (torch.empty_like(q).pin_memory(), torch.empty_like(k).pin_memory(), torch.empty_like(v).pin_memory())
     fa_backward_host(p, q, k, v, o, do, L, *out, workspace, heads_per_group, stream)
     return out
 

@@ -189,7 +189,8 @@ template <typename T, int HD, bool kSlices>
 __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict__ acc, T* __restrict__ dQ, int H,
                                                          int N, int64_t sb, int64_t sh, int64_t sn,
                                                          int tiles_per_head, float scale, int slices,
-                                                         int64_t slice_elems, int causal, int kb_rows) {
+                                                         int64_t slice_elems, int causal, int kb_rows,
+                                                         int64_t offset) {
   constexpr int kPitch = HD + 4;  // floats; keeps 16-byte alignment, staggers banks
   extern __shared__ float4 smem_f4[];
   float* tile_s = reinterpret_cast<float*>(smem_f4);
@@ -198,11 +199,12 @@ __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict
   const int b = bh / H, h = bh % H;
   const float4* src = reinterpret_cast<const float4*>(acc + dq_unit_offset(bh, tiles_per_head, tile, 0, 0, HD));
   // Key blocks that touch this query tile: all, or (causal) those starting at
-  // or before its last row.  Their slices are summed in increasing order.
+  // or before the last key its last row sees (row + offset, offset = N_k - N);
+  // none when that is negative.  Their slices are summed in increasing order.
   int last = slices - 1;
-  if (causal && slices > 1) {
-    const int lim = (tile * kTileRows + kTileRows - 1) / kb_rows;
-    last = lim < last ? lim : last;
+  if (kSlices && causal) {
+    const int64_t hi = (int64_t)tile * kTileRows + kTileRows - 1 + offset;
+    last = hi < 0 ? -1 : (hi / kb_rows < last ? (int)(hi / kb_rows) : last);
   }
   const int64_t slice4 = slice_elems / 4;
   // a tile is 4 x (HD/16) units of [4 column groups][32 rows][4 columns]
@@ -210,7 +212,8 @@ __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict
   for (int k = threadIdx.x; k < kTileRows * HD / 4; k += 256) {
     const int unit = k / 128, g = (k % 128) / 32, r = k % 32;
     const int row = (unit / (HD / 16)) * 32 + r, col = (unit % (HD / 16)) * 16 + g * 4;
-    float4 v = __ldg(src + k);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!kSlices || last >= 0) v = __ldg(src + k);
     if (kSlices)
       for (int sl = 1; sl <= last; ++sl) {
         const float4 w = __ldg(src + sl * slice4 + k);
@@ -248,7 +251,8 @@ static cudaError_t launch_convert_t(const fa_problem& p, const float* acc, T* dQ
       if (e != cudaSuccess) return e;                                                                      \
     }                                                                                                      \
     kern<<<grid, 256, sm, s>>>(acc, dQ, p.H, p.N, p.stride_b, p.stride_h, p.stride_n, tiles, p.scale,      \
-                               (int)dq_slices(p), dq_slice_elems(p), p.causal, key_block_rows(p));         \
+                               (int)dq_slices(p), dq_slice_elems(p), p.causal, key_block_rows(p),          \
+                               causal_offset(p));                                                          \
     break;                                                                                                 \
   }
   switch (p.d) {
@@ -303,17 +307,19 @@ namespace {
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-fa_status validate(const fa_problem* p) {
-  if (!p) return FA_ERR_INVALID_ARG;
-  if (p->B < 1 || p->H < 1 || p->N < 1 || p->d < 1) return FA_ERR_INVALID_ARG;
+fa_status validate_normalized(const fa_problem* p) {
+  if (p->B < 1 || p->H < 1 || p->N < 1 || p->N_k < 1 || p->d < 1) return FA_ERR_INVALID_ARG;
+  if (p->reserved != 0) return FA_ERR_INVALID_ARG;
   if (p->flags & ~(int32_t)FA_FLAG_DETERMINISTIC) return FA_ERR_INVALID_ARG;
   if (p->causal != 0 && p->causal != 1) return FA_ERR_INVALID_ARG;
   if (!(p->scale == p->scale) || p->scale <= 0.f || p->scale > 1e30f) return FA_ERR_INVALID_ARG;
   if (p->dtype != FA_BF16 && p->dtype != FA_FP32) return FA_ERR_INVALID_ARG;
-  if (p->N > (1 << 24) || (int64_t)p->B * p->H > (1 << 24)) return FA_ERR_UNSUPPORTED;
+  if (p->N > (1 << 24) || p->N_k > (1 << 24) || (int64_t)p->B * p->H > (1 << 24)) return FA_ERR_UNSUPPORTED;
   const int64_t es = p->dtype == FA_BF16 ? 2 : 4;
   if (p->stride_n < p->d || p->stride_h < 1 || p->stride_b < 1) return FA_ERR_INVALID_ARG;
   if ((p->stride_n * es) % 16 || (p->stride_h * es) % 16 || (p->stride_b * es) % 16) return FA_ERR_INVALID_ARG;
+  if (p->kstride_n < p->d || p->kstride_h < 1 || p->kstride_b < 1) return FA_ERR_INVALID_ARG;
+  if ((p->kstride_n * es) % 16 || (p->kstride_h * es) % 16 || (p->kstride_b * es) % 16) return FA_ERR_INVALID_ARG;
   if (p->dtype == FA_BF16) {
     if (p->d != 32 && p->d != 64 && p->d != 96 && p->d != 128 && p->d != 256) return FA_ERR_UNSUPPORTED;
   } else {
@@ -323,62 +329,87 @@ fa_status validate(const fa_problem* p) {
   return FA_OK;
 }
 
+// Validates *in and writes its normalised form (N_k = 0: self-attention,
+// N_k = N with the Q strides) to *out.
+fa_status normalize(const fa_problem* in, fa_problem* out) {
+  if (!in) return FA_ERR_INVALID_ARG;
+  if (in->N_k < 0) return FA_ERR_INVALID_ARG;
+  *out = *in;
+  if (in->N_k == 0) {
+    out->N_k = in->N;
+    out->kstride_b = in->stride_b;
+    out->kstride_h = in->stride_h;
+    out->kstride_n = in->stride_n;
+  }
+  return validate_normalized(out);
+}
+
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 }  // namespace
 
+namespace fa {
+bool normalize_problem(const fa_problem* in, fa_problem* out) { return normalize(in, out) == FA_OK; }
+}  // namespace fa
+
 extern "C" {
 
 size_t fa_dq_accum_elems(const fa_problem* p) {
-  if (validate(p) != FA_OK) return 0;
-  return (size_t)(fa::dq_slices(*p) * fa::dq_slice_elems(*p));
+  fa_problem pn;
+  if (normalize(p, &pn) != FA_OK) return 0;
+  return (size_t)(fa::dq_slices(pn) * fa::dq_slice_elems(pn));
 }
 
 fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* V, void* O, float* L,
                  void* stream) {
-  fa_status st = validate(p);
+  fa_problem pn;
+  fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(L)) return FA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (!fa::tensor_core(*p)) return from_cuda(fa::launch_fwd_simt(*p, Q, K, V, O, L, s));
+  if (!fa::tensor_core(pn)) return from_cuda(fa::launch_fwd_simt(pn, Q, K, V, O, L, s));
   int32_t* status = fa::device_status_word();
   if (!status) return FA_ERR_CUDA;
-  return from_cuda(fa::launch_fwd_sm103(*p, Q, K, V, O, L, status, fa::wait_limit_ns(), s));
+  return from_cuda(fa::launch_fwd_sm103(pn, Q, K, V, O, L, status, fa::wait_limit_ns(), s));
 }
 
 fa_status fa_bwd_preprocess(const fa_problem* p, const void* O, const void* dO, float* D, float* dQ_accum,
                             void* stream) {
-  fa_status st = validate(p);
+  fa_problem pn;
+  fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
   if (!aligned16(O) || !aligned16(dO) || !aligned16(D) || !aligned16(dQ_accum)) return FA_ERR_INVALID_ARG;
-  return from_cuda(fa::launch_preprocess(*p, O, dO, D, dQ_accum, (cudaStream_t)stream));
+  return from_cuda(fa::launch_preprocess(pn, O, dO, D, dQ_accum, (cudaStream_t)stream));
 }
 
 fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* V, const void* dO, const float* L,
                  const float* D, float* dQ_accum, void* dK, void* dV, void* stream) {
-  fa_status st = validate(p);
+  fa_problem pn;
+  fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(L) || !aligned16(D) ||
       !aligned16(dQ_accum) || !aligned16(dK) || !aligned16(dV))
     return FA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (!fa::tensor_core(*p)) return from_cuda(fa::launch_bwd_simt(*p, Q, K, V, dO, L, D, dQ_accum, dK, dV, s));
+  if (!fa::tensor_core(pn)) return from_cuda(fa::launch_bwd_simt(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, s));
   int32_t* status = fa::device_status_word();
   if (!status) return FA_ERR_CUDA;
-  return from_cuda(fa::launch_bwd_sm103(*p, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s));
+  return from_cuda(fa::launch_bwd_sm103(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s));
 }
 
 fa_status fa_convert_dq(const fa_problem* p, const float* dQ_accum, void* dQ, void* stream) {
-  fa_status st = validate(p);
+  fa_problem pn;
+  fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
   if (!aligned16(dQ_accum) || !aligned16(dQ)) return FA_ERR_INVALID_ARG;
-  return from_cuda(fa::launch_convert_dq(*p, dQ_accum, dQ, (cudaStream_t)stream));
+  return from_cuda(fa::launch_convert_dq(pn, dQ_accum, dQ, (cudaStream_t)stream));
 }
 
 fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const void* V, const void* O,
                       const void* dO, const float* L, float* D, float* dQ_accum, void* dQ, void* dK, void* dV,
                       void* stream) {
-  fa_status st = validate(p);
+  fa_problem pn;
+  fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
   if (!aligned16(dQ)) return FA_ERR_INVALID_ARG;
   st = fa_bwd_preprocess(p, O, dO, D, dQ_accum, stream);

@@ -128,9 +128,12 @@ struct BwdParams {
   __nv_bfloat16* dV;
   int32_t* status;
   uint64_t wait_ns;
-  int B, H, N;
-  int n_tiles;  // ceil(N / 128), for both queries and keys
-  int64_t sb, sh, sn;
+  int B, H, N, Nk;      // query rows, key rows
+  int n_tiles;          // ceil(N / 128): query blocks (and dQ accumulator tiles)
+  int nk_tiles;         // ceil(Nk / 128): key blocks, one CTA each per head
+  int offset;           // Nk - N: key j visible to query i iff j <= i + offset (causal)
+  int64_t sb, sh, sn;   // Q-shaped strides
+  int64_t ksb, ksh, ksn;  // K-shaped strides (dK, dV written with these)
   float scale;
   int causal;
   int64_t slice_elems;  // > 0: deterministic, key block kb stores into slice kb
@@ -180,7 +183,9 @@ __device__ __forceinline__ void store_row(uint32_t taddr, bool valid, __nv_bfloa
   }
 }
 
-template <int HD, bool kDet>
+// kRect: causal with N_k != N (the mask is offset from the diagonal); a
+// separate instantiation so that the square case keeps its cheaper loop.
+template <int HD, bool kDet, bool kRect>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -233,13 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // other so the CTAs resident at any time share a few heads' Q, dO and dQ
   // accumulator in L2; inside a head, key block 0 (the longest causal walk)
   // comes first.
-  const int kb = blockIdx.x % prm.n_tiles;
-  const int bh = blockIdx.x / prm.n_tiles;
+  const int kb = blockIdx.x % prm.nk_tiles;
+  const int bh = blockIdx.x / prm.nk_tiles;
   const int b = bh / prm.H, h = bh % prm.H;
   const int k0 = kb * kBlk;
-  const int q_first = prm.causal ? kb : 0;
+  // first query block holding a query that sees key k0: i >= k0 - offset
+  // (every key block has one, the last query sees every key)
+  const int q_first = !prm.causal ? 0 : !kRect ? kb : (k0 > prm.offset ? (k0 - prm.offset) / kBlk : 0);
   const int n_iter = prm.n_tiles - q_first;
-  const int64_t head = (int64_t)b * prm.sb + (int64_t)h * prm.sh;
+  const int64_t khead = (int64_t)b * prm.ksb + (int64_t)h * prm.ksh;
   const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
 
   const uint32_t sK = sbase + Ly::kK, sV = sbase + Ly::kV, sdS = sbase + Ly::kdS;
@@ -412,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = qq * 32 + lane;          // TMEM lane
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
     const int kr = k0 + t;                 // key row of S, dP, dV, dK
-    const bool key_ok = kr < prm.N;
+    const bool key_ok = kr < prm.Nk;
+    const int kd = kRect ? k0 - prm.offset : k0;  // key k0 + t visible to query q iff q - kd >= t
     const float sl2 = prm.scale * kLog2e;
     const int c0 = G * 32;                 // query columns [c0, c0 + 32) of S, dP
     // this warp's dQ columns [G * kCols, +kCols): d = 128, 64 all four
@@ -515,7 +523,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         ptx::tmem_ld32(tm + Ly::kColS + lane_off + c0, r);
         const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4 + c0 * 4;
-        const bool diag = prm.causal && q0 == k0;
+        // key k0 + t is visible to query q0 + col iff col >= t - rel; the
+        // block needs the mask unless every entry passes (rel >= 127).
+        // Square problems: rel = 0 on the diagonal block only.
+        const int rel = kRect ? q0 - kd : 0;
+        const bool diag = prm.causal && (kRect ? rel < kBlk - 1 : q0 == k0);
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
           const float4 l4 = ptx::ld_shared_f4(sLa + j * 4);
@@ -523,12 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
           float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
           float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
-          if (diag) {  // key k0 + t is visible to query q0 + col iff t <= col
+          if (diag) {
             const int col = c0 + j;
-            p0 = col + 0 < t ? 0.f : p0;
-            p1 = col + 1 < t ? 0.f : p1;
-            p2 = col + 2 < t ? 0.f : p2;
-            p3 = col + 3 < t ? 0.f : p3;
+            const int lim = t - rel;  // masked iff col < lim
+            p0 = col + 0 < lim ? 0.f : p0;
+            p1 = col + 1 < lim ? 0.f : p1;
+            p2 = col + 2 < lim ? 0.f : p2;
+            p3 = col + 3 < lim ? 0.f : p3;
           }
           pk[j / 2] = ptx::pack_bf16x2(p0, p1);
           pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
@@ -599,9 +612,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kHalf = HD / 2;        // warps G = 0, 1 store dV, G = 2, 3 store dK
       const int cc = (G & 1) * kHalf;
       if (G < 2)
-        store_row<kHalf>(tm + Ly::kColdV + lane_off + cc, key_ok, prm.dV + head + (int64_t)kr * prm.sn + cc, 1.0f);
+        store_row<kHalf>(tm + Ly::kColdV + lane_off + cc, key_ok, prm.dV + khead + (int64_t)kr * prm.ksn + cc, 1.0f);
       else
-        store_row<kHalf>(tm + Ly::kColdK + lane_off + cc, key_ok, prm.dK + head + (int64_t)kr * prm.sn + cc,
+        store_row<kHalf>(tm + Ly::kColdK + lane_off + cc, key_ok, prm.dK + khead + (int64_t)kr * prm.ksn + cc,
                          prm.scale);
     }
   }
@@ -614,15 +627,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int HD, bool kDet>
+template <int HD, bool kDet, bool kRect>
 cudaError_t launch_hd(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t s) {
   using Ly = Layout<(HD <= 64 ? 64 : 128)>;
   cudaError_t e =
-      cudaFuncSetAttribute(bwd_sm103_kernel<HD, kDet>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+      cudaFuncSetAttribute(bwd_sm103_kernel<HD, kDet, kRect>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
-  bwd_sm103_kernel<HD, kDet><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  const dim3 grid((unsigned)((int64_t)prm.nk_tiles * p.B * p.H));
+  bwd_sm103_kernel<HD, kDet, kRect><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_d(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, bool det, bool rect,
+                     cudaStream_t s) {
+  if (det) return rect ? launch_hd<HD, true, true>(p, maps, prm, s) : launch_hd<HD, true, false>(p, maps, prm, s);
+  return rect ? launch_hd<HD, false, true>(p, maps, prm, s) : launch_hd<HD, false, false>(p, maps, prm, s);
 }
 
 }  // namespace
@@ -643,13 +663,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-// [B, H, N, d] bf16 tensor as a 4-D TMA map with 64 x 128 boxes, 128-byte
-// swizzle; rows past N read as zeros.
-bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p) {
+// A Q-shaped [B, H, N, d] (kv = false) or K-shaped [B, H, N_k, d] (kv = true)
+// bf16 tensor as a 4-D TMA map with 64 x 128 boxes, 128-byte swizzle; rows
+// past the end and columns past d read as zeros.
+bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p, bool kv) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.N, (cuuint64_t)p.H, (cuuint64_t)p.B};
-  cuuint64_t strides[3] = {(cuuint64_t)p.stride_n * 2, (cuuint64_t)p.stride_h * 2, (cuuint64_t)p.stride_b * 2};
+  const int64_t rows = kv ? p.N_k : p.N;
+  const int64_t sn = kv ? p.kstride_n : p.stride_n, sh = kv ? p.kstride_h : p.stride_h;
+  const int64_t sb = kv ? p.kstride_b : p.stride_b;
+  cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)rows, (cuuint64_t)p.H, (cuuint64_t)p.B};
+  cuuint64_t strides[3] = {(cuuint64_t)sn * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
   cuuint32_t box[4] = {64, (cuuint32_t)kBlk, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
@@ -662,8 +686,8 @@ cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, 
                              const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
                              uint64_t wait_ns, cudaStream_t s) {
   CUtensorMap maps[4];
-  if (!make_bf16_tile_map(&maps[0], Q, p) || !make_bf16_tile_map(&maps[1], K, p) ||
-      !make_bf16_tile_map(&maps[2], V, p) || !make_bf16_tile_map(&maps[3], dO, p))
+  if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
+      !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false))
     return cudaErrorInvalidValue;
   BwdParams prm;
   prm.L = L;
@@ -676,19 +700,26 @@ cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, 
   prm.B = p.B;
   prm.H = p.H;
   prm.N = p.N;
+  prm.Nk = p.N_k;
   prm.n_tiles = (int)ceil_div(p.N, kBlk);
+  prm.nk_tiles = (int)ceil_div(p.N_k, kBlk);
+  prm.offset = (int)causal_offset(p);
   prm.sb = p.stride_b;
   prm.sh = p.stride_h;
   prm.sn = p.stride_n;
+  prm.ksb = p.kstride_b;
+  prm.ksh = p.kstride_h;
+  prm.ksn = p.kstride_n;
   prm.scale = p.scale;
   prm.causal = p.causal;
   prm.slice_elems = deterministic(p) ? dq_slice_elems(p) : 0;
   const bool det = prm.slice_elems > 0;
+  const bool rect = p.causal && prm.offset != 0;
   switch (p.d) {
-    case 32: return det ? launch_hd<32, true>(p, maps, prm, s) : launch_hd<32, false>(p, maps, prm, s);
-    case 64: return det ? launch_hd<64, true>(p, maps, prm, s) : launch_hd<64, false>(p, maps, prm, s);
-    case 96: return det ? launch_hd<96, true>(p, maps, prm, s) : launch_hd<96, false>(p, maps, prm, s);
-    case 128: return det ? launch_hd<128, true>(p, maps, prm, s) : launch_hd<128, false>(p, maps, prm, s);
+    case 32: return launch_d<32>(p, maps, prm, det, rect, s);
+    case 64: return launch_d<64>(p, maps, prm, det, rect, s);
+    case 96: return launch_d<96>(p, maps, prm, det, rect, s);
+    case 128: return launch_d<128>(p, maps, prm, det, rect, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -44,7 +44,7 @@
 
 namespace fa {
 
-bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p);  // fa_bwd_sm103.cu
+bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p, bool kv);  // fa_bwd_sm103.cu
 
 namespace {
 
@@ -105,6 +105,8 @@ struct FwdParams {
   int64_t sb, sh, sn;
   float scale;
   int causal;
+  int Nk, nk_tiles;  // key rows, key blocks
+  int offset;        // Nk - N: key j visible to query i iff j <= i + offset (causal)
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const ptx::Waiter& w) {
@@ -155,7 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = prm.n_tiles - 1 - blockIdx.x % prm.n_tiles;
   const int b = bh / prm.H, h = bh % prm.H;
   const int q0 = qt * kBlk;
-  const int n_blk = prm.causal ? qt + 1 : prm.n_tiles;
+  // key blocks this query block sees: all, or (causal) up to the last key its
+  // last row sees; none if even that row sees no key
+  int n_blk = prm.nk_tiles;
+  if (prm.causal) {
+    const int hi = min(q0 + kBlk - 1, prm.N - 1) + prm.offset;
+    n_blk = hi < 0 ? 0 : min(prm.nk_tiles, hi / kBlk + 1);
+  }
   const int64_t head = (int64_t)b * prm.sb + (int64_t)h * prm.sh;
   const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
   const uint32_t sQ = sbase + Ly::kQ;
@@ -191,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0, forwarded = 0;
     if (lane == 0) {
       ptx::prefetch_tensormap(map);
-      if (isK) {
+      if (isK && n_blk > 0) {
         ptx::prefetch_tensormap(&tmQ);
         ptx::mbar_arrive_expect_tx(bar(Q_FULL), Ly::kTile);
 #pragma unroll
@@ -220,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) {
       // shared memory must not be released under copies still in flight
-      if (isK) ptx::wait_bounded(bar(Q_FULL), 0, W, false);
+      if (isK && n_blk > 0) ptx::wait_bounded(bar(Q_FULL), 0, W, false);
       for (int j = forwarded; j < issued; ++j) ptx::wait_bounded(bar(full0 + j % nst), (j / nst) & 1, W, false);
     }
   } else if (warp == 9) {
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    bool ok = warp_wait(bar(Q_FULL), 0, W) && issue_S(0);
+    bool ok = n_blk == 0 || (warp_wait(bar(Q_FULL), 0, W) && issue_S(0));
     if (ok && n_blk > 1) ok = issue_S(1);
     for (int j = 0; ok && j < n_blk; ++j) {
       const int sb = j % kSBufs, vs = j % kVStages;
@@ -298,11 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t r[64];
       ptx::tmem_ld64(tS + lane_off + c0, tS + lane_off + c0 + 32, r);
       const int k0 = j * kBlk + c0;
-      if ((prm.causal && j == qt) || (j * kBlk + kBlk > prm.N)) {
-        // columns c >= lim of this warp's 64 are masked (past N, or later
-        // than the query under the causal mask)
-        int lim = prm.N - k0;
-        if (prm.causal) lim = min(lim, qrow - k0 + 1);
+      if ((prm.causal && j * kBlk + kBlk - 1 > q0 + prm.offset) || (j * kBlk + kBlk > prm.Nk)) {
+        // columns c >= lim of this warp's 64 are masked (past N_k, or later
+        // than the query's last visible key under the causal mask)
+        int lim = prm.Nk - k0;
+        if (prm.causal) lim = min(lim, qrow + prm.offset - k0 + 1);
 #pragma unroll
         for (int c = 0; c < 64; ++c) r[c] = c < lim ? r[c] : __float_as_uint(-INFINITY);
       }
@@ -360,35 +368,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       xchg[(4 + G) * kBlk + t] = l_part;
       named_bar_sync(1 + qq, 64);
       const float l = l_part + xchg[(4 + (G ^ 1)) * kBlk + t];
-      if (warp_wait(bar(O_DONE0 + (n_blk - 1) % kSBufs), ((n_blk - 1) / kSBufs) & 1, W)) {
+      // A row that sees no key (l = 0; every row of a block with n_blk = 0,
+      // whose O in tensor memory was never written) stores O = 0, L = +inf.
+      if (n_blk == 0 || warp_wait(bar(O_DONE0 + (n_blk - 1) % kSBufs), ((n_blk - 1) / kSBufs) & 1, W)) {
         ptx::tc_fence_after();
-        const float inv = 1.f / l;
+        const bool empty = !(l > 0.f);
+        const float inv = empty ? 0.f : 1.f / l;
         constexpr int kOC = HD / 2;
         __nv_bfloat16* orow = prm.O + head + (int64_t)qrow * prm.sn + G * kOC;
         // 32-column pieces, then a 16-column tail (d = 32, 96)
         auto put = [&](const uint32_t* o, int n, int c) {
 #pragma unroll
           for (int u = 0; u < n / 8; ++u) {
-            uint4 v;
-            v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
-            v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
-            v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
-            v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (!empty) {
+              v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
+              v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
+              v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
+              v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
+            }
             *reinterpret_cast<uint4*>(orow + c + 8 * u) = v;
           }
         };
 #pragma unroll
         for (int c = 0; c + 32 <= kOC; c += 32) {
           uint32_t o[32];
-          ptx::tmem_ld32(tm + Ly::kColO + lane_off + G * kOC + c, o);
+          if (n_blk > 0) ptx::tmem_ld32(tm + Ly::kColO + lane_off + G * kOC + c, o);
           if (qrow < prm.N) put(o, 32, c);
         }
         if constexpr (kOC % 32 == 16) {
           uint32_t o[16];
-          ptx::tmem_ld16(tm + Ly::kColO + lane_off + G * kOC + kOC - 16, o);
+          if (n_blk > 0) ptx::tmem_ld16(tm + Ly::kColO + lane_off + G * kOC + kOC - 16, o);
           if (qrow < prm.N) put(o, 16, kOC - 16);
         }
-        if (G == 0 && qrow < prm.N) prm.L[(int64_t)bh * prm.N + qrow] = (m_run + log2f(l)) * kLn2;
+        if (G == 0 && qrow < prm.N)
+          prm.L[(int64_t)bh * prm.N + qrow] = empty ? INFINITY : (m_run + log2f(l)) * kLn2;
       }
     }
   }
@@ -416,8 +430,8 @@ cudaError_t launch_fwd_hd(const fa_problem& p, const CUtensorMap* maps, const Fw
 cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                              int32_t* status, uint64_t wait_ns, cudaStream_t s) {
   CUtensorMap maps[3];
-  if (!make_bf16_tile_map(&maps[0], Q, p) || !make_bf16_tile_map(&maps[1], K, p) ||
-      !make_bf16_tile_map(&maps[2], V, p))
+  if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
+      !make_bf16_tile_map(&maps[2], V, p, true))
     return cudaErrorInvalidValue;
   FwdParams prm;
   prm.O = (__nv_bfloat16*)O;
@@ -428,6 +442,9 @@ cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, 
   prm.H = p.H;
   prm.N = p.N;
   prm.n_tiles = (int)ceil_div(p.N, kBlk);
+  prm.Nk = p.N_k;
+  prm.nk_tiles = (int)ceil_div(p.N_k, kBlk);
+  prm.offset = (int)causal_offset(p);
   prm.sb = p.stride_b;
   prm.sh = p.stride_h;
   prm.sn = p.stride_n;

@@ -56,16 +56,18 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct SlotLayout {
   size_t q, k, v, o, dO, dq, dk, dv, L, D, acc, bytes;
 };
+// p is normalised (N_k set).
 SlotLayout slot_layout(const fa_problem& p, int g) {
   const size_t es = p.dtype == FA_BF16 ? 2 : 4;
-  const size_t head = (size_t)p.N * p.d * es;
+  const size_t qhead = (size_t)p.N * p.d * es, khead = (size_t)p.N_k * p.d * es;
   const size_t rows = (size_t)g * p.N * 4;
   const size_t acc = (size_t)g * ceil_div(p.N, kTileRows) * kTileRows * p.d * 4 * dq_slices(p);
   SlotLayout s;
   size_t off = 0;
   for (size_t* f : {&s.q, &s.k, &s.v, &s.o, &s.dO, &s.dq, &s.dk, &s.dv}) {
     *f = off;
-    off += align256(g * head);
+    const bool kshaped = f == &s.k || f == &s.v || f == &s.dk || f == &s.dv;
+    off += align256(g * (kshaped ? khead : qhead));
   }
   s.L = off;
   off += align256(rows);
@@ -88,31 +90,35 @@ int default_group(const fa_problem& p) {
 extern "C" {
 
 size_t fa_backward_host_workspace_bytes(const fa_problem* p, int32_t heads_per_group) {
-  if (fa_dq_accum_elems(p) == 0) return 0;
-  const int g = heads_per_group > 0 ? heads_per_group : fa::default_group(*p);
-  return fa::kSlots * fa::slot_layout(*p, g).bytes;
+  fa_problem pn;
+  if (!fa::normalize_problem(p, &pn)) return 0;
+  const int g = heads_per_group > 0 ? heads_per_group : fa::default_group(pn);
+  return fa::kSlots * fa::slot_layout(pn, g).bytes;
 }
 
 fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, const void* hV, const void* hO,
                            const void* hdO, const float* hL, void* hdQ, void* hdK, void* hdV, void* workspace,
                            size_t workspace_bytes, int32_t heads_per_group, void* stream) {
-  if (fa_dq_accum_elems(p) == 0) return p ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARG;
+  fa_problem pn;
+  if (!fa::normalize_problem(p, &pn)) return p ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARG;
   if (!hQ || !hK || !hV || !hO || !hdO || !hL || !hdQ || !hdK || !hdV || !workspace) return FA_ERR_INVALID_ARG;
   if (heads_per_group < 0) return FA_ERR_INVALID_ARG;
-  // host tensors are dense [B, H, N, d]
-  if (p->stride_n != p->d || p->stride_h != (int64_t)p->N * p->d || p->stride_b != (int64_t)p->H * p->N * p->d)
+  // host tensors are dense [B, H, N, d] and [B, H, N_k, d]
+  if (pn.stride_n != pn.d || pn.stride_h != (int64_t)pn.N * pn.d || pn.stride_b != (int64_t)pn.H * pn.N * pn.d ||
+      pn.kstride_n != pn.d || pn.kstride_h != (int64_t)pn.N_k * pn.d ||
+      pn.kstride_b != (int64_t)pn.H * pn.N_k * pn.d)
     return FA_ERR_INVALID_ARG;
-  const int heads = p->B * p->H;
-  const int g = heads_per_group > 0 ? (heads_per_group < heads ? heads_per_group : heads) : fa::default_group(*p);
-  const fa::SlotLayout lay = fa::slot_layout(*p, g);
+  const int heads = pn.B * pn.H;
+  const int g = heads_per_group > 0 ? (heads_per_group < heads ? heads_per_group : heads) : fa::default_group(pn);
+  const fa::SlotLayout lay = fa::slot_layout(pn, g);
   if (workspace_bytes < fa::kSlots * lay.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return FA_ERR_INVALID_ARG;
   fa::HostPipe* hp = fa::pipe_for_current_device();
   if (!hp) return FA_ERR_CUDA;
   cudaStream_t cs = (cudaStream_t)stream;
-  const size_t es = p->dtype == FA_BF16 ? 2 : 4;
-  const size_t head_bytes = (size_t)p->N * p->d * es;
-  const size_t row_bytes = (size_t)p->N * 4;
+  const size_t es = pn.dtype == FA_BF16 ? 2 : 4;
+  const size_t qhead_bytes = (size_t)pn.N * pn.d * es, khead_bytes = (size_t)pn.N_k * pn.d * es;
+  const size_t row_bytes = (size_t)pn.N * 4;
   auto H2D = cudaMemcpyHostToDevice;
   auto D2H = cudaMemcpyDeviceToHost;
 
@@ -125,13 +131,16 @@ fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, 
     const int h0 = c * g;
     const int gh = heads - h0 < g ? heads - h0 : g;
     uint8_t* base = static_cast<uint8_t*>(workspace) + s * lay.bytes;
-    const size_t off = (size_t)h0 * head_bytes, n = (size_t)gh * head_bytes;
+    const size_t qoff = (size_t)h0 * qhead_bytes, qn = (size_t)gh * qhead_bytes;
+    const size_t koff = (size_t)h0 * khead_bytes, kn = (size_t)gh * khead_bytes;
     // copy in (the slot's previous group must have been copied out)
     if (c >= fa::kSlots) e = cudaStreamWaitEvent(hp->in, hp->ev_out[s], 0);
     const void* srcs[5] = {hQ, hK, hV, hO, hdO};
     const size_t dsts[5] = {lay.q, lay.k, lay.v, lay.o, lay.dO};
+    const bool ksh[5] = {false, true, true, false, false};
     for (int t = 0; t < 5 && e == cudaSuccess; ++t)
-      e = cudaMemcpyAsync(base + dsts[t], static_cast<const uint8_t*>(srcs[t]) + off, n, H2D, hp->in);
+      e = cudaMemcpyAsync(base + dsts[t], static_cast<const uint8_t*>(srcs[t]) + (ksh[t] ? koff : qoff),
+                          ksh[t] ? kn : qn, H2D, hp->in);
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(base + lay.L, reinterpret_cast<const uint8_t*>(hL) + (size_t)h0 * row_bytes,
                           (size_t)gh * row_bytes, H2D, hp->in);
@@ -139,10 +148,15 @@ fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, 
     // compute on the caller's stream
     if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, hp->ev_in[s], 0);
     if (e != cudaSuccess) break;
-    fa_problem pc = *p;
+    fa_problem pc = pn;  // the group: B = 1, H = gh, dense slots
     pc.B = 1;
     pc.H = gh;
-    pc.stride_b = (int64_t)gh * p->N * p->d;
+    pc.stride_n = pn.d;
+    pc.stride_h = (int64_t)pn.N * pn.d;
+    pc.stride_b = (int64_t)gh * pn.N * pn.d;
+    pc.kstride_n = pn.d;
+    pc.kstride_h = (int64_t)pn.N_k * pn.d;
+    pc.kstride_b = (int64_t)gh * pn.N_k * pn.d;
     fa_status st = fa_backward(&pc, base + lay.q, base + lay.k, base + lay.v, base + lay.o, base + lay.dO,
                                reinterpret_cast<const float*>(base + lay.L), reinterpret_cast<float*>(base + lay.D),
                                reinterpret_cast<float*>(base + lay.acc), base + lay.dq, base + lay.dk,
@@ -154,7 +168,8 @@ fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, 
     void* outs[3] = {hdQ, hdK, hdV};
     const size_t srcs_out[3] = {lay.dq, lay.dk, lay.dv};
     for (int t = 0; t < 3 && e == cudaSuccess; ++t)
-      e = cudaMemcpyAsync(static_cast<uint8_t*>(outs[t]) + off, base + srcs_out[t], n, D2H, hp->out);
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(outs[t]) + (t ? koff : qoff), base + srcs_out[t], t ? kn : qn, D2H,
+                          hp->out);
     if (e == cudaSuccess) e = cudaEventRecord(hp->ev_out[s], hp->out);
   }
   // the caller's stream continues only after the last copy out

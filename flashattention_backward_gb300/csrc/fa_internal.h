@@ -25,6 +25,15 @@ int32_t* device_status_word();
 uint64_t wait_limit_ns();
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// floor(a / b) for b > 0 and any sign of a
+inline int64_t floor_div(int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Every launcher below takes a problem normalised by the API layer: N_k > 0
+// and the kstride fields set (N_k = 0 in a caller's fa_problem means N_k = N
+// with the Q strides).  Causal offset: key j is visible to query i iff
+// j <= i + causal_offset(p).
+bool normalize_problem(const fa_problem* in, fa_problem* out);  // false: invalid or unsupported
+inline int64_t causal_offset(const fa_problem& p) { return (int64_t)p.N_k - p.N; }
 
 inline bool deterministic(const fa_problem& p) { return (p.flags & FA_FLAG_DETERMINISTIC) != 0; }
 // bf16 with d <= 128 runs on the tensor-core kernels; fp32, and bf16 with
@@ -36,7 +45,7 @@ inline bool tensor_core(const fa_problem& p) { return p.dtype == FA_BF16 && p.d 
 inline int key_block_rows(const fa_problem& p) { return tensor_core(p) ? 128 : (p.d == 256 ? 32 : 64); }
 // dQ accumulator slices: one per key block in deterministic mode, else one.
 inline int64_t dq_slices(const fa_problem& p) {
-  return deterministic(p) ? ceil_div(p.N, key_block_rows(p)) : 1;
+  return deterministic(p) ? ceil_div(p.N_k, key_block_rows(p)) : 1;
 }
 // Floats in one slice: B * H * ceil(N/128) * 128 * d.
 inline int64_t dq_slice_elems(const fa_problem& p) {

@@ -62,7 +62,10 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict__ Q, const T* __restrict__ K,
                                                             const T* __restrict__ V, T* __restrict__ O,
                                                             float* __restrict__ L, int H, int N, int64_t sb,
-                                                            int64_t sh, int64_t sn, float scale, int causal) {
+                                                            int64_t sh, int64_t sn, float scale, int causal,
+                                                            int Nk, int64_t ksb, int64_t ksh, int64_t ksn) {
+  // Q, O: N rows with strides (sb, sh, sn); K, V: Nk rows with (ksb, ksh,
+  // ksn).  Causal: key j visible to query i iff j <= i + Nk - N.
   constexpr int kPQ = HD + 1, kPV = HD, kPP = kT + 1;
   constexpr int kCols = HD / 16;
   extern __shared__ float smem[];
@@ -72,10 +75,13 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict_
   float* sP = sV + kT * kPV;
 
   const int tiles = (N + kT - 1) / kT;
+  const int k_tiles = (Nk + kT - 1) / kT;
+  const int offset = Nk - N;
   const int qt = blockIdx.x % tiles;
   const int bh = blockIdx.x / tiles;
   const int b = bh / H, h = bh % H;
   const int64_t head = (int64_t)b * sb + (int64_t)h * sh;
+  const int64_t khead = (int64_t)b * ksb + (int64_t)h * ksh;
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
   const int q0 = qt * kT;
   const float sl2 = scale * kLog2e;
@@ -91,12 +97,16 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict_
     for (int u = 0; u < kCols; ++u) acc[a][u] = 0.f;
   }
 
-  const int kt_end = causal ? qt + 1 : tiles;
+  int kt_end = k_tiles;
+  if (causal) {  // up to the last key the tile's last row sees
+    const int hi = min(q0 + kT - 1, N - 1) + offset;
+    kt_end = hi < 0 ? 0 : min(k_tiles, hi / kT + 1);
+  }
   for (int kt = 0; kt < kt_end; ++kt) {
     const int k0 = kt * kT;
     __syncthreads();  // previous tile's sK/sV/sP reads are done
-    load_tile<T, HD>(sK, kPQ, K + head, sn, k0, N);
-    load_tile<T, HD>(sV, kPV, V + head, sn, k0, N);
+    load_tile<T, HD>(sK, kPQ, K + khead, ksn, k0, Nk);
+    load_tile<T, HD>(sV, kPV, V + khead, ksn, k0, Nk);
     __syncthreads();
 
     float s[4][4];
@@ -123,7 +133,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict_
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
         const int j = k0 + tx + 16 * bb;
-        const bool masked = (j >= N) || (causal && j > i);
+        const bool masked = (j >= Nk) || (causal && j > i + offset);
         s[a][bb] = masked ? -INFINITY : s[a][bb] * sl2;
         rmax = fmaxf(rmax, s[a][bb]);
       }
@@ -162,11 +172,12 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const T* __restrict_
   for (int a = 0; a < 4; ++a) {
     const int i = q0 + ty + 16 * a;
     if (i >= N) continue;
-    const float inv = 1.f / l[a];
+    const bool empty = !(l[a] > 0.f);  // no visible key: O = 0, L = +inf
+    const float inv = empty ? 0.f : 1.f / l[a];
     T* orow = O + head + (int64_t)i * sn;
 #pragma unroll
-    for (int u = 0; u < kCols; ++u) from_f(orow + tx + 16 * u, acc[a][u] * inv);
-    if (tx == 0) L[(int64_t)bh * N + i] = (m[a] + log2f(l[a])) * kLn2;
+    for (int u = 0; u < kCols; ++u) from_f(orow + tx + 16 * u, empty ? 0.f : acc[a][u] * inv);
+    if (tx == 0) L[(int64_t)bh * N + i] = empty ? INFINITY : (m[a] + log2f(l[a])) * kLn2;
   }
 }
 
@@ -180,9 +191,11 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
     const float* __restrict__ Lg, const float* __restrict__ Dg, float* __restrict__ dq_accum, T* __restrict__ dK,
     T* __restrict__ dV, int H, int N, int64_t sb, int64_t sh, int64_t sn, float scale, int causal,
-    int64_t slice_elems) {
+    int64_t slice_elems, int Nk, int64_t ksb, int64_t ksh, int64_t ksn) {
   // slice_elems > 0 (deterministic): this key block's dQ contributions are
   // stored into its own slice of the accumulator instead of added.
+  // Q, dO: N rows with strides (sb, sh, sn); K, V, dK, dV: Nk rows with
+  // (ksb, ksh, ksn).  Causal: key j visible to query i iff j <= i + Nk - N.
   constexpr int kP = HD + 1, kPP = KT + 1;
   constexpr int kR = KT / 16;   // rows (and columns) of a tile per thread
   constexpr int kCols = HD / 16;
@@ -196,18 +209,21 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
   float* sL = sdS + KT * kPP;  // L * log2(e), +inf for rows >= N
   float* sD = sL + KT;
 
-  const int tiles = (N + KT - 1) / KT;
-  const int kb = blockIdx.x % tiles;
-  const int bh = blockIdx.x / tiles;
+  const int tiles = (N + KT - 1) / KT;       // query tiles
+  const int k_tiles = (Nk + KT - 1) / KT;    // key blocks, one per block of threads
+  const int offset = Nk - N;
+  const int kb = blockIdx.x % k_tiles;
+  const int bh = blockIdx.x / k_tiles;
   const int b = bh / H, h = bh % H;
   const int64_t head = (int64_t)b * sb + (int64_t)h * sh;
+  const int64_t khead = (int64_t)b * ksb + (int64_t)h * ksh;
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
   const int k0 = kb * KT;
   const float sl2 = scale * kLog2e;
   const int acc_tiles = (N + kTileRows - 1) / kTileRows;
 
-  load_tile<T, HD, KT>(sK, kP, K + head, sn, k0, N);
-  load_tile<T, HD, KT>(sV, kP, V + head, sn, k0, N);
+  load_tile<T, HD, KT>(sK, kP, K + khead, ksn, k0, Nk);
+  load_tile<T, HD, KT>(sV, kP, V + khead, ksn, k0, Nk);
 
   float dv[kR][kCols], dk[kR][kCols];
 #pragma unroll
@@ -215,7 +231,9 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
 #pragma unroll
     for (int u = 0; u < kCols; ++u) dv[a][u] = dk[a][u] = 0.f;
 
-  for (int qt = causal ? kb : 0; qt < tiles; ++qt) {
+  // first query tile holding a query that sees key k0: i >= k0 - offset
+  const int qt_first = causal && k0 > offset ? (k0 - offset) / KT : 0;
+  for (int qt = qt_first; qt < tiles; ++qt) {
     const int q0 = qt * KT;
     __syncthreads();
     load_tile<T, HD, KT>(sQ, kP, Q + head, sn, q0, N);
@@ -259,7 +277,7 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
 #pragma unroll
       for (int bb = 0; bb < kR; ++bb) {
         const int jl = tx + 16 * bb, j = k0 + jl;
-        const bool masked = (j >= N) || (causal && j > i);
+        const bool masked = (j >= Nk) || (causal && j > i + offset);
         const float p = masked ? 0.f : ptx::ex2(fmaf(s[a][bb], sl2, -sL[il]));
         sP[il * kPP + jl] = p;
         sdS[il * kPP + jl] = p * (dp[a][bb] - sD[il]);
@@ -321,12 +339,12 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
 #pragma unroll
   for (int a = 0; a < kR; ++a) {
     const int j = k0 + ty + 16 * a;
-    if (j >= N) continue;
+    if (j >= Nk) continue;
 #pragma unroll
     for (int u = 0; u < kCols; ++u) {
       const int c = tx + 16 * u;
-      from_f(dV + head + (int64_t)j * sn + c, dv[a][u]);
-      from_f(dK + head + (int64_t)j * sn + c, scale * dk[a][u]);
+      from_f(dV + khead + (int64_t)j * ksn + c, dv[a][u]);
+      from_f(dK + khead + (int64_t)j * ksn + c, scale * dk[a][u]);
     }
   }
 }
@@ -345,7 +363,8 @@ cudaError_t launch_fwd_t(const fa_problem& p, const T* Q, const T* K, const T* V
   const int tiles = (p.N + kT - 1) / kT;
   const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
   fwd_simt_kernel<T, HD><<<grid, kThreads, sm, s>>>(Q, K, V, O, L, p.H, p.N, p.stride_b, p.stride_h, p.stride_n,
-                                                   p.scale, p.causal);
+                                                   p.scale, p.causal, p.N_k, p.kstride_b, p.kstride_h,
+                                                   p.kstride_n);
   return cudaGetLastError();
 }
 
@@ -374,11 +393,12 @@ cudaError_t launch_bwd_t(const fa_problem& p, const void* Q, const void* K, cons
   const size_t sm = sizeof(float) * (size_t)(4 * KT * (HD + 1) + 2 * KT * (KT + 1) + 2 * KT);
   cudaError_t e = set_smem(bwd_simt_kernel<T, HD, KT>, sm);
   if (e != cudaSuccess) return e;
-  const int tiles = (p.N + KT - 1) / KT;
-  const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
+  const int k_tiles = (p.N_k + KT - 1) / KT;
+  const dim3 grid((unsigned)((int64_t)p.B * p.H * k_tiles));
   bwd_simt_kernel<T, HD, KT><<<grid, kThreads, sm, s>>>(
       (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, L, D, acc, (T*)dK, (T*)dV, p.H, p.N, p.stride_b,
-      p.stride_h, p.stride_n, p.scale, p.causal, deterministic(p) ? dq_slice_elems(p) : 0);
+      p.stride_h, p.stride_n, p.scale, p.causal, deterministic(p) ? dq_slice_elems(p) : 0, p.N_k, p.kstride_b,
+      p.kstride_h, p.kstride_n);
   return cudaGetLastError();
 }
 

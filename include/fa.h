@@ -18,9 +18,11 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Q, K, V, O, dO, dQ, dK, dV are [B, H, N, d] tensors of `dtype` with the
- *    last dimension contiguous and element strides stride_b, stride_h,
- *    stride_n (identical for all eight tensors).  N_q == N_k == N.
+ *  - Q, O, dO, dQ are [B, H, N, d] and K, V, dK, dV [B, H, N_k, d] tensors of
+ *    `dtype` with the last dimension contiguous and element strides
+ *    (stride_b, stride_h, stride_n), respectively (kstride_b, kstride_h,
+ *    kstride_n); N_k = 0 in fa_problem means N_k = N with one set of strides
+ *    for all eight tensors (self-attention, the case the pages describe).
  *  - L and D are dense [B, H, N] float32 arrays (row-major, no padding).
  *  - The dQ accumulator is a float32 array of fa_dq_accum_elems() elements in
  *    a tile-blocked layout (below).  It belongs to the caller like every
@@ -41,11 +43,13 @@
  *    reach the accumulator in whatever order the hardware completes its
  *    reductions (the FA2 default; ch.16 §16.3 notes deterministic=False).
  *
- * Supported problems: dtype FA_BF16 with d in {32, 64, 96, 128} (tcgen05
+ * Supported problems (N is the number of query rows, N_k of key rows; see
+ * fa_problem): dtype FA_BF16 with d in {32, 64, 96, 128} (tcgen05
  * tensor-core kernels) or d = 256 (CUDA-core kernels with fp32 arithmetic:
  * at d = 256 the dK and dV accumulators alone would fill tensor memory);
  * dtype FA_FP32 with d in {16, 32, 64, 96, 128, 256} (exact fp32 FFMA
- * kernels, no TF32).  N >= 1, B >= 1, H >= 1, N <= 2^24, B*H <= 2^24.
+ * kernels, no TF32).  N >= 1, N_k >= 0, B >= 1, H >= 1, N, N_k <= 2^24,
+ * B*H <= 2^24.
  * Other d return FA_ERR_UNSUPPORTED.
  *
  * dQ accumulator layout
@@ -96,20 +100,34 @@ typedef enum {
   FA_FLAG_DETERMINISTIC = 1
 } fa_flags;
 
+/* Shapes: Q, O, dO, dQ are [B, H, N, d] with strides (stride_b, stride_h,
+ * stride_n); K, V, dK, dV are [B, H, N_k, d] with strides (kstride_b,
+ * kstride_h, kstride_n); L and D are dense [B, H, N] float32.  N_k = 0 means
+ * self-attention, N_k = N with the K/V strides equal to the Q strides (the
+ * kstride fields are then ignored).
+ *
+ * Causal mask (N_k != N is not covered by the source pages, which show only
+ * N_q == N_k): aligned bottom-right, key j is visible to query i iff
+ * j <= i + (N_k - N); at N_k == N this is the pages' j <= i.  A query that
+ * sees no key (only possible when N > N_k) gets O = 0, L = +inf and zero
+ * gradients. */
 typedef struct {
   int32_t B, H, N, d;
   float scale;      /* softmax scale, normally 1/sqrt(d) */
-  int32_t causal;   /* 1: key j visible to query i iff j <= i (top-left) */
+  int32_t causal;   /* 1: key j visible to query i iff j <= i + N_k - N */
   int32_t dtype;    /* fa_dtype of Q, K, V, O, dO, dQ, dK, dV */
   int32_t flags;    /* fa_flags bits (0: default mode); other bits must be 0 */
-  int64_t stride_b, stride_h, stride_n; /* element strides; d is contiguous */
+  int64_t stride_b, stride_h, stride_n; /* element strides of Q-shaped tensors; d is contiguous */
+  int32_t N_k;      /* key/value rows; 0: equal to N (self-attention) */
+  int32_t reserved; /* must be 0 */
+  int64_t kstride_b, kstride_h, kstride_n; /* element strides of K-shaped tensors (N_k > 0) */
 } fa_problem;
 
 /* Number of float32 elements of the dQ accumulator for problem p, or 0 if p
  * is NULL or invalid: B * H * ceil(N/128) * 128 * d, times the number of key
- * blocks with FA_FLAG_DETERMINISTIC: ceil(N/128) on the tensor-core kernels
- * (bf16, d <= 128), ceil(N/64) on the CUDA-core kernels, ceil(N/32) on those
- * at d = 256. */
+ * blocks with FA_FLAG_DETERMINISTIC: ceil(N_k/128) on the tensor-core kernels
+ * (bf16, d <= 128), ceil(N_k/64) on the CUDA-core kernels, ceil(N_k/32) on
+ * those at d = 256. */
 size_t fa_dq_accum_elems(const fa_problem* p);
 
 /* Forward pass, companion of the backward: O = softmax(scale Q K^T) V and
@@ -152,8 +170,9 @@ fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const v
                       float* dQ_accum, void* dQ, void* dK, void* dV, void* stream);
 
 /* Backward pass for tensors in host memory (page-locked for overlap):
- * Q, K, V, O, dO, dQ, dK, dV dense [B, H, N, d] host arrays (stride_n = d,
- * stride_h = N*d, stride_b = H*N*d), L a dense [B, H, N] float32 host array.
+ * Q, O, dO, dQ dense [B, H, N, d] and K, V, dK, dV dense [B, H, N_k, d] host
+ * arrays (p's strides must say so: stride_n = d, stride_h = rows*d,
+ * stride_b = H*rows*d), L a dense [B, H, N] float32 host array.
  * Heads are independent, so the batch streams through `workspace` (device
  * memory, 256-byte aligned, at least fa_backward_host_workspace_bytes()) in
  * groups of `heads_per_group` heads (0: about four groups): group c+1 is

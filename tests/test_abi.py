@@ -67,6 +67,15 @@ def test_dq_accum_size(lib):
     assert fa.fa_dq_accum_elems(p) == 4 * 128 * 256
     p = _prob(N=100, d=96, H=1, stride_b=100 * 96, stride_h=100 * 96, stride_n=96, flags=fa.FA_FLAG_DETERMINISTIC)
     assert fa.fa_dq_accum_elems(p) == 1 * 128 * 96
+    # N_k != N: one accumulator tile per 128 query rows, one slice per key block
+    p = _prob(N=100, N_k=300, kstride_b=2 * 300 * 64, kstride_h=300 * 64, kstride_n=64)
+    assert fa.fa_dq_accum_elems(p) == 2 * 128 * 64
+    p = _prob(N=100, N_k=300, kstride_b=2 * 300 * 64, kstride_h=300 * 64, kstride_n=64,
+              flags=fa.FA_FLAG_DETERMINISTIC)
+    assert fa.fa_dq_accum_elems(p) == 3 * 2 * 128 * 64
+    p = _prob(N=100, N_k=300, kstride_b=2 * 300 * 64, kstride_h=300 * 64, kstride_n=64, dtype=fa.FA_FP32,
+              flags=fa.FA_FLAG_DETERMINISTIC)
+    assert fa.fa_dq_accum_elems(p) == 5 * 2 * 128 * 64
 
 
 BAD = 0x1000  # a 16-byte aligned dummy address; validation fails before any use
@@ -81,6 +90,12 @@ BAD = 0x1000  # a 16-byte aligned dummy address; validation fails before any use
         (dict(d=16, stride_n=16), fa.FA_ERR_UNSUPPORTED),
         (dict(d=512, stride_n=512), fa.FA_ERR_UNSUPPORTED),
         (dict(d=80, stride_n=80, dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),
+        (dict(N_k=-1), fa.FA_ERR_INVALID_ARG),
+        (dict(reserved=1), fa.FA_ERR_INVALID_ARG),
+        (dict(N_k=50), fa.FA_ERR_INVALID_ARG),  # K strides left at 0
+        (dict(N_k=50, kstride_b=2 * 50 * 64, kstride_h=50 * 64, kstride_n=60), fa.FA_ERR_INVALID_ARG),
+        (dict(N_k=50, kstride_b=2 * 50 * 64, kstride_h=50 * 64, kstride_n=68), fa.FA_ERR_INVALID_ARG),
+        (dict(N_k=(1 << 24) + 1, kstride_b=64, kstride_h=64, kstride_n=64), fa.FA_ERR_UNSUPPORTED),
         (dict(causal=2), fa.FA_ERR_INVALID_ARG),
         (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
         (dict(flags=2), fa.FA_ERR_INVALID_ARG),
