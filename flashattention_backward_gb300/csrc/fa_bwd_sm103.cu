@@ -69,6 +69,7 @@ constexpr int kProducerWarp = kComputeWarps;
 constexpr int kMmaWarp = kComputeWarps + 1;  // on the same SM sub-partition as lane quarter 1
 constexpr int kThreads = 32 * (kComputeWarps + 2);
 constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kHeadGroup = 4;  // heads whose key blocks interleave in the grid order
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum BarId {
@@ -234,12 +235,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tm = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
-  // work item: key block kb of head (b, h).  Heads are walked one after the
-  // other so the CTAs resident at any time share a few heads' Q, dO and dQ
-  // accumulator in L2; inside a head, key block 0 (the longest causal walk)
-  // comes first.
-  const int kb = blockIdx.x % prm.nk_tiles;
-  const int bh = blockIdx.x / prm.nk_tiles;
+  // work item: key block kb of head (b, h).  Heads are taken in groups of
+  // kHeadGroup so the CTAs resident at any time share a few heads' Q, dO and
+  // dQ accumulator in L2; inside a group the key blocks go round the heads,
+  // key block 0 (the longest causal walk) first, so the short walks of the
+  // last group fill the SMs at the end of the grid.
+  const int bh_total = prm.B * prm.H;
+  const int grp = blockIdx.x / (kHeadGroup * prm.nk_tiles);
+  const int gsize = min(kHeadGroup, bh_total - grp * kHeadGroup);
+  const int r = blockIdx.x - grp * kHeadGroup * prm.nk_tiles;
+  const int kb = r / gsize;
+  const int bh = grp * kHeadGroup + r % gsize;
   const int b = bh / prm.H, h = bh % prm.H;
   const int k0 = kb * kBlk;
   // first query block holding a query that sees key k0: i >= k0 - offset
