@@ -54,6 +54,7 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kKStages = 3;  // K tiles in shared memory
 constexpr int kVStages = 2;  // V tiles in shared memory
 constexpr int kSBufs = 3;    // S/P buffers in TMEM
+constexpr int kHeadGroup = 4;  // heads whose query blocks interleave in the grid order
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -151,10 +152,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tm = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
-  // work item: query block qt of head (b, h); heads one after another (K, V
-  // of a head shared in L2), the longest causal walk first inside a head
-  const int bh = blockIdx.x / prm.n_tiles;
-  const int qt = prm.n_tiles - 1 - blockIdx.x % prm.n_tiles;
+  // work item: query block qt of head (b, h).  Heads are taken in groups of
+  // kHeadGroup (K, V of a few heads shared in L2); inside a group the query
+  // blocks go round the heads, the last (longest causal walk) first, so the
+  // short walks of the last group fill the SMs at the end of the grid.
+  const int bh_total = prm.B * prm.H;
+  const int grp = blockIdx.x / (kHeadGroup * prm.n_tiles);
+  const int gsize = min(kHeadGroup, bh_total - grp * kHeadGroup);
+  const int r = blockIdx.x - grp * kHeadGroup * prm.n_tiles;
+  const int bh = grp * kHeadGroup + r % gsize;
+  const int qt = prm.n_tiles - 1 - r / gsize;
   const int b = bh / prm.H, h = bh % prm.H;
   const int q0 = qt * kBlk;
   // key blocks this query block sees: all, or (causal) up to the last key its
