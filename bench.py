@@ -306,6 +306,28 @@ def main(argv=None) -> int:
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     cvt_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
+    # the same step as one launch (fa_backward_fused), timed after the timed
+    # region for comparison; the three launches above are faster on this GPU
+    fused = None
+    sync_n = fa.fa_backward_fused_sync_elems(p)
+    if sync_n > 0:
+        sync = torch.empty(sync_n, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            fa.fa_backward_fused(p, q, k, v, o, g, L, D, acc, sync, dq, dk, dv, stream)
+        n_fused = max(5, args.steps // 10)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n_fused):
+            fa.fa_backward_fused(p, q, k, v, o, g, L, D, acc, sync, dq, dk, dv, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if fa.get_device_status() != 0:
+            raise RuntimeError("device status set by the single-launch backward")
+        fused_ms = e0.elapsed_time(e1) / n_fused
+        fused = {"ms": fused_ms, "TFLOPS": w.counted_flops / (fused_ms * 1e-3) / 1e12,
+                 "note": "preprocess + bwd + convert in one launch; not the step timed above"}
+
     # end to end through the public API with host buffers: fa_backward_host
     # streams groups of heads through a device workspace, copies overlapped
     # with compute; every input crosses host->device and every gradient
@@ -373,6 +395,7 @@ def main(argv=None) -> int:
             "fa_bwd": {"ms": bwd_ms, "TFLOPS": bwd_tflops},
             "fa_convert_dq": {"ms": cvt_ms, "GB/s": cvt_bytes / (cvt_ms * 1e-3) / 1e9,
                               "frac_hbm": cvt_bytes / (cvt_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+            "fa_backward_fused": fused,
             "fa_fwd": {"ms": statistics.mean(fwd_ms),
                        "TFLOPS": 0.4 * flops / (statistics.mean(fwd_ms) * 1e-3) / 1e12,
                        "note": "companion forward, not part of the step; 4 B H N^2 d (half if causal)"},

@@ -105,6 +105,10 @@ def load_library() -> ctypes.CDLL:
     lib.fa_backward.argtypes = [P, vp, vp, vp, vp, vp, fp, fp, fp, vp, vp, vp, vp]
     for name in ("fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_convert_dq", "fa_backward"):
         getattr(lib, name).restype = st
+    lib.fa_backward_fused_sync_elems.argtypes = [P]
+    lib.fa_backward_fused_sync_elems.restype = ctypes.c_size_t
+    lib.fa_backward_fused.argtypes = [P] + [vp] * 13
+    lib.fa_backward_fused.restype = st
     lib.fa_backward_host_workspace_bytes.argtypes = [P, ctypes.c_int32]
     lib.fa_backward_host_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_backward_host.argtypes = [P] + [vp] * 9 + [vp, ctypes.c_size_t, ctypes.c_int32, vp]
@@ -260,6 +264,23 @@ def fa_backward(p: FaProblem, q, k, v, o, do, L, D, dq_accum, dq, dk, dv, stream
            "fa_backward")
 
 
+def fa_backward_fused_sync_elems(p: FaProblem) -> int:
+    return int(load_library().fa_backward_fused_sync_elems(ctypes.byref(p)))
+
+
+def fa_backward_fused(p: FaProblem, q, k, v, o, do, L, D, dq_accum, sync, dq, dk, dv, stream=None) -> None:
+    """fa_backward in a single kernel launch (tensor-core problems only)."""
+    _same_layout(p, q, o, do, dq)
+    _k_layout(p, k, v, dk, dv)
+    _rows(p, L, D)
+    _accum(p, dq_accum)
+    if sync.dtype != torch.int32 or not sync.is_cuda or sync.numel() < fa_backward_fused_sync_elems(p):
+        raise ValueError("sync must be an int32 CUDA tensor of fa_backward_fused_sync_elems() elements")
+    _check(load_library().fa_backward_fused(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(L),
+                                            _ptr(D), _ptr(dq_accum), _ptr(sync), _ptr(dq), _ptr(dk), _ptr(dv),
+                                            _stream(stream)), "fa_backward_fused")
+
+
 def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
     """O, L for [B, H, N, d] queries and [B, H, N_k, d] keys/values (CUDA, bf16
     or fp32; last dimension contiguous)."""
@@ -271,16 +292,22 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
 
 
 def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, stream=None, workspace=None,
-                       deterministic: bool = False):
-    """dQ, dK, dV.  ``workspace`` may pass preallocated (D, dq_accum)."""
+                       deterministic: bool = False, fused: bool = False):
+    """dQ, dK, dV.  ``workspace`` may pass preallocated (D, dq_accum) or, with
+    ``fused`` (one kernel launch, tensor-core problems), (D, dq_accum, sync)."""
     p = problem_for(q, scale, causal, deterministic, k=k)
     if workspace is None:
         D = torch.empty((p.B, p.H, p.N), dtype=torch.float32, device=q.device)
         acc = torch.empty(fa_dq_accum_elems(p), dtype=torch.float32, device=q.device)
+        sync = torch.empty(fa_backward_fused_sync_elems(p) if fused else 0, dtype=torch.int32, device=q.device)
     else:
-        D, acc = workspace
+        D, acc = workspace[0], workspace[1]
+        sync = workspace[2] if fused else None
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_backward(p, q, k, v, o, do, L, D, acc, dq, dk, dv, stream)
+    if fused:
+        fa_backward_fused(p, q, k, v, o, do, L, D, acc, sync, dq, dk, dv, stream)
+    else:
+        fa_backward(p, q, k, v, o, do, L, D, acc, dq, dk, dv, stream)
     return dq, dk, dv
 
 

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "dq_layout.cuh"
+#include "row_dot.cuh"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -51,70 +52,31 @@ uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 // shuffles.  The same block then zeroes that tile of the accumulator
 // (128 * d floats, float4 stores).  Pure HBM streaming.
 // ----------------------------------------------------------------------------
-template <typename T>
-struct Vec16;
-template <>
-struct Vec16<float> {
-  static constexpr int kElems = 4;
-  __device__ static float dot(const uint4& a, const uint4& b) {
-    return __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
-           __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
-  }
-};
-template <>
-struct Vec16<__nv_bfloat16> {
-  static constexpr int kElems = 8;
-  __device__ static float dot2(uint32_t a, uint32_t b) {
-    float a0 = __uint_as_float(a << 16), a1 = __uint_as_float(a & 0xffff0000u);
-    float b0 = __uint_as_float(b << 16), b1 = __uint_as_float(b & 0xffff0000u);
-    return a0 * b0 + a1 * b1;
-  }
-  __device__ static float dot(const uint4& a, const uint4& b) {
-    return dot2(a.x, b.x) + dot2(a.y, b.y) + dot2(a.z, b.z) + dot2(a.w, b.w);
-  }
-};
-
 template <typename T, int HD>
 __global__ void __launch_bounds__(256) preprocess_kernel(const T* __restrict__ O, const T* __restrict__ dO,
                                                          float* __restrict__ D, float* __restrict__ dq_accum,
                                                          int H, int N, int64_t sb, int64_t sh, int64_t sn,
                                                          int tiles_per_head, int zero_slices,
                                                          int64_t slice_elems) {
-  constexpr int kVec = Vec16<T>::kElems;
-  constexpr int kVecs = HD / kVec;                 // 16-byte vectors per row: 2 .. 64
-  // lanes per row: a power of two (lanes past kVecs idle), at most 32; each
-  // lane takes vectors sub, sub + kLanesPerRow, ...
-  constexpr int kLanesPerRow = kVecs <= 2 ? 2 : kVecs <= 4 ? 4 : kVecs <= 8 ? 8 : kVecs <= 16 ? 16 : 32;
-  constexpr int kPerLane = (kVecs + kLanesPerRow - 1) / kLanesPerRow;
-  constexpr int kRowsPerStep = 256 / kLanesPerRow;
+  using RD = RowDot<T, HD>;
+  constexpr int kRowsPerStep = 256 / RD::kLanes;
   constexpr int kSteps = kTileRows / kRowsPerStep;
   const int tile = blockIdx.x % tiles_per_head;
   const int bh = blockIdx.x / tiles_per_head;
   const int b = bh / H, h = bh % H;
-  const int sub = threadIdx.x % kLanesPerRow;
-  const int row_in_step = threadIdx.x / kLanesPerRow;
+  const int sub = threadIdx.x % RD::kLanes;
+  const int row_in_step = threadIdx.x / RD::kLanes;
   const int64_t head_off = (int64_t)b * sb + (int64_t)h * sh;
 
   float acc[kSteps];
 #pragma unroll
   for (int s = 0; s < kSteps; ++s) {
     const int n = tile * kTileRows + s * kRowsPerStep + row_in_step;
-    acc[s] = 0.f;
-#pragma unroll
-    for (int v = 0; v < kPerLane; ++v) {
-      const int vec = sub + v * kLanesPerRow;
-      if (n < N && vec < kVecs) {
-        const int64_t off = head_off + (int64_t)n * sn + vec * kVec;
-        const uint4 a = __ldg(reinterpret_cast<const uint4*>(O + off));
-        const uint4 g = __ldg(reinterpret_cast<const uint4*>(dO + off));
-        acc[s] += Vec16<T>::dot(a, g);
-      }
-    }
+    acc[s] = n < N ? RD::partial(O + head_off + (int64_t)n * sn, dO + head_off + (int64_t)n * sn, sub) : 0.f;
   }
 #pragma unroll
   for (int s = 0; s < kSteps; ++s) {
-#pragma unroll
-    for (int m = kLanesPerRow / 2; m > 0; m >>= 1) acc[s] += __shfl_xor_sync(0xffffffffu, acc[s], m);
+    acc[s] = RD::reduce(acc[s]);
     const int n = tile * kTileRows + s * kRowsPerStep + row_in_step;
     if (sub == 0 && n < N) D[(int64_t)bh * N + n] = acc[s];
   }
@@ -417,6 +379,30 @@ fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const v
   st = fa_bwd(p, Q, K, V, dO, L, D, dQ_accum, dK, dV, stream);
   if (st != FA_OK) return st;
   return fa_convert_dq(p, dQ_accum, dQ, stream);
+}
+
+size_t fa_backward_fused_sync_elems(const fa_problem* p) {
+  fa_problem pn;
+  if (normalize(p, &pn) != FA_OK || !fa::tensor_core(pn)) return 0;
+  return 1 + 2 * (size_t)pn.B * pn.H;
+}
+
+fa_status fa_backward_fused(const fa_problem* p, const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* L, float* D, float* dQ_accum, int32_t* sync, void* dQ,
+                            void* dK, void* dV, void* stream) {
+  fa_problem pn;
+  fa_status st = normalize(p, &pn);
+  if (st != FA_OK) return st;
+  if (!fa::tensor_core(pn)) return FA_ERR_UNSUPPORTED;
+  if (fa::fused_items(pn) > 0x7fffffff) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(L) ||
+      !aligned16(D) || !aligned16(dQ_accum) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV) || !sync ||
+      (reinterpret_cast<uintptr_t>(sync) & 3u))
+    return FA_ERR_INVALID_ARG;
+  int32_t* status = fa::device_status_word();
+  if (!status) return FA_ERR_CUDA;
+  return from_cuda(fa::launch_bwd_fused_sm103(pn, Q, K, V, O, dO, L, D, dQ_accum, sync, dQ, dK, dV, status,
+                                              fa::wait_limit_ns(), (cudaStream_t)stream));
 }
 
 fa_status fa_get_device_status(void* stream, int32_t* code) {

@@ -57,6 +57,7 @@
 #include <type_traits>
 
 #include "dq_layout.cuh"
+#include "row_dot.cuh"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -184,13 +185,31 @@ __device__ __forceinline__ void store_row(uint32_t taddr, bool valid, __nv_bfloa
   }
 }
 
+// Bounded wait until *c >= target (acquire, GPU scope), polled by one thread.
+__device__ __forceinline__ bool wait_counter(const int32_t* c, int target, uint64_t limit_ns) {
+  const uint64_t t0 = ptx::globaltimer();
+  for (;;) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= target) return true;
+    if (ptx::globaltimer() - t0 > limit_ns) return false;
+    __nanosleep(256);
+  }
+}
+
+// The backward for one key block kb of head bh, run by a whole CTA.
 // kRect: causal with N_k != N (the mask is offset from the diagonal); a
 // separate instantiation so that the square case keeps its cheaper loop.
-template <int HD, bool kDet, bool kRect>
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                     const BwdParams prm) {
+// ready (may be null): before any load, wait (bounded) until *ready >=
+// ready_target, i.e. until D and the zeroed accumulator of this head have
+// been published.  done (may be null): once every dQ contribution of this
+// block has reached global memory, add 1 (release).
+// kFused: run inside the single-launch backward (ready and done are used,
+// D is read coherently since this launch writes it); otherwise both are null.
+template <int HD, bool kDet, bool kRect, bool kFused>
+__device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                          const CUtensorMap& tmdO, const BwdParams& prm, const int kb, const int bh,
+                                          const int32_t* ready, int ready_target, int32_t* done) {
   constexpr int LD = HD <= 64 ? 64 : 128;
   using Ly = Layout<LD>;
   constexpr int kDoSt = Ly::kDoStages;
@@ -234,18 +253,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tm = __shfl_sync(0xffffffffu, *tmem_slot, 0);
+  if (kFused) {
+    if (threadIdx.x == 0) {
+      if (!wait_counter(ready, ready_target, prm.wait_ns)) {
+        *abort_flag = 1;
+        atomicCAS(prm.status, 0, (int32_t)FA_ERR_TIMEOUT);
+      }
+      // the zeros were written by generic stores; the TMA's bulk reductions
+      // (async proxy) must come after them
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncthreads();
+    if (*abort_flag) {  // nothing was started: free tensor memory and leave
+      if (warp == kMmaWarp) ptx::tmem_dealloc(tm, Ly::kTmemCols);
+      return;
+    }
+  }
 
-  // work item: key block kb of head (b, h).  Heads are taken in groups of
-  // kHeadGroup so the CTAs resident at any time share a few heads' Q, dO and
-  // dQ accumulator in L2; inside a group the key blocks go round the heads,
-  // key block 0 (the longest causal walk) first, so the short walks of the
-  // last group fill the SMs at the end of the grid.
-  const int bh_total = prm.B * prm.H;
-  const int grp = blockIdx.x / (kHeadGroup * prm.nk_tiles);
-  const int gsize = min(kHeadGroup, bh_total - grp * kHeadGroup);
-  const int r = blockIdx.x - grp * kHeadGroup * prm.nk_tiles;
-  const int kb = r / gsize;
-  const int bh = grp * kHeadGroup + r % gsize;
   const int b = bh / prm.H, h = bh % prm.H;
   const int k0 = kb * kBlk;
   // first query block holding a query that sees key k0: i >= k0 - offset
@@ -284,7 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < kBlk / 32; ++u) {
         const int q = q0 + lane + 32 * u;
         lv[u] = q < prm.N ? __ldg(prm.L + (int64_t)bh * prm.N + q) * kLog2e : INFINITY;
-        dv[u] = q < prm.N ? __ldg(prm.D + (int64_t)bh * prm.N + q) : 0.f;
+        // D may have been written earlier in this launch: read it at L2
+        dv[u] = q < prm.N ? (kFused ? __ldcg(prm.D + (int64_t)bh * prm.N + q) : __ldg(prm.D + (int64_t)bh * prm.N + q))
+                          : 0.f;
       }
     };
     fetch_rows(0);
@@ -611,7 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       issue_reds(Lo{});
       issue_reds(Hi{});
     }
-    if (lane == 0) ptx::bulk_wait_all();  // this warp's bulk operations are complete
+    if (lane == 0) {
+      ptx::bulk_wait_all();  // this warp's bulk operations are complete
+      if (kFused) asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     __syncwarp();
     if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
       ptx::tc_fence_after();
@@ -625,12 +654,253 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (kFused) __threadfence();  // this thread's reductions and stores before the release
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tm, Ly::kTmemCols);
   }
+  if (kFused && threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(done, 1);
+  }
+}
+
+template <int HD, bool kDet, bool kRect>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const BwdParams prm) {
+  // work item: key block kb of head (b, h).  Heads are taken in groups of
+  // kHeadGroup so the CTAs resident at any time share a few heads' Q, dO and
+  // dQ accumulator in L2; inside a group the key blocks go round the heads,
+  // key block 0 (the longest causal walk) first, so the short walks of the
+  // last group fill the SMs at the end of the grid.
+  const int bh_total = prm.B * prm.H;
+  const int grp = blockIdx.x / (kHeadGroup * prm.nk_tiles);
+  const int gsize = min(kHeadGroup, bh_total - grp * kHeadGroup);
+  const int r = blockIdx.x - grp * kHeadGroup * prm.nk_tiles;
+  bwd_block<HD, kDet, kRect, false>(tmQ, tmK, tmV, tmdO, prm, r / gsize, grp * kHeadGroup + r % gsize, nullptr, 0,
+                                    nullptr);
+}
+
+// ---------------------------------------------------------------------------
+// Single-launch backward: preprocess (D, zeroed accumulator), the key blocks
+// and convert as items of one grid.  Each CTA takes a ticket in the order
+// CTAs start, and the ticket names its item; an item only waits for items
+// with smaller tickets (started, so resident or finished), so no wait can
+// depend on a CTA that has not been scheduled.  Order, with heads in groups
+// of kHeadGroup:  P(0), then for each group k: P(k+1), B(k), C(k-1); last
+// C(G-1).  P = D and the zeroed accumulator of kTilesPerItem 128-row query
+// tiles, B = one key block (waits until every P of its head is done), C =
+// the dQ conversion of kTilesPerItem query tiles (waits until every B of its
+// head is done).
+// ---------------------------------------------------------------------------
+enum : int { kItemPre = 0, kItemBwd = 1, kItemCvt = 2 };
+constexpr int kTilesPerItem = 8;  // query tiles per P and per C item
+
+struct FusedParams {
+  const __nv_bfloat16* O;
+  const __nv_bfloat16* dO;
+  __nv_bfloat16* dQ;
+  float* D;
+  // [0] ticket; [1, 1 + BH) P items done per head; [1 + BH, 1 + 2 BH) B items
+  // done per head; zeroed before the launch
+  int32_t* sync;
+};
+
+// Ticket t -> (role, bh, idx): idx is the item of query tiles (P, C; T items
+// per head) or the key block (B; Tk per head).
+__host__ __device__ inline void fused_item(int64_t t, int BH, int T, int Tk, int& role, int& bh, int& idx) {
+  const int G = (BH + kHeadGroup - 1) / kHeadGroup;
+  auto gs = [&](int g) { return BH - kHeadGroup * g < kHeadGroup ? BH - kHeadGroup * g : kHeadGroup; };
+  auto sp = [&](int k) -> int64_t { return k + 1 < G ? (int64_t)gs(k + 1) * T : 0; };
+  auto sb = [&](int k) -> int64_t { return (int64_t)gs(k) * Tk; };
+  auto sc = [&](int k) -> int64_t { return k >= 1 ? (int64_t)gs(k - 1) * T : 0; };
+  auto in_slot = [&](int k, int64_t o) {
+    if (o < sp(k)) {
+      role = kItemPre;
+      bh = kHeadGroup * (k + 1) + (int)(o / T);
+      idx = (int)(o % T);
+      return;
+    }
+    o -= sp(k);
+    if (o < sb(k)) {  // key blocks go round the heads of the group, block 0 first
+      role = kItemBwd;
+      bh = kHeadGroup * k + (int)(o % gs(k));
+      idx = (int)(o / gs(k));
+      return;
+    }
+    o -= sb(k);
+    role = kItemCvt;
+    bh = kHeadGroup * (k - 1) + (int)(o / T);
+    idx = (int)(o % T);
+  };
+  const int64_t p0 = (int64_t)gs(0) * T;
+  if (t < p0) {
+    role = kItemPre;
+    bh = (int)(t / T);
+    idx = (int)(t % T);
+    return;
+  }
+  t -= p0;
+  int k = 0;
+  // slots 1 .. full - 2 only involve full groups: one size, skipped by division
+  const int full = BH / kHeadGroup;
+  const int64_t s0 = sp(0) + sb(0) + sc(0);
+  if (t < s0) return in_slot(0, t);
+  t -= s0;
+  k = 1;
+  if (full >= 3) {
+    const int64_t U = (int64_t)kHeadGroup * (2 * (int64_t)T + Tk);
+    const int64_t nu = full - 2;
+    if (t < nu * U) return in_slot(1 + (int)(t / U), t % U);
+    t -= nu * U;
+    k = full - 1;
+  }
+  for (; k < G; ++k) {
+    const int64_t sk = sp(k) + sb(k) + sc(k);
+    if (t < sk) return in_slot(k, t);
+    t -= sk;
+  }
+  role = kItemCvt;  // C(G - 1)
+  bh = kHeadGroup * (G - 1) + (int)(t / T);
+  idx = (int)(t % T);
+}
+
+// P item: D for query rows [tile * 128, +128) of head bh (computed exactly as
+// the preprocess kernel does, see row_dot.cuh), and the accumulator tile
+// zeroed.
+template <int HD>
+__device__ __forceinline__ void pre_tile(const BwdParams& prm, const FusedParams& fp, int bh, int tile, bool zero) {
+  using RD = RowDot<__nv_bfloat16, HD>;
+  constexpr int kRowsPerStep = kComputeThreads / RD::kLanes;
+  const int b = bh / prm.H, h = bh % prm.H;
+  const int64_t head = (int64_t)b * prm.sb + (int64_t)h * prm.sh;
+  if (threadIdx.x < kComputeThreads) {
+    const int sub = threadIdx.x % RD::kLanes, row_in_step = threadIdx.x / RD::kLanes;
+#pragma unroll
+    for (int r0 = 0; r0 < kBlk; r0 += kRowsPerStep) {
+      const int n = tile * kBlk + r0 + row_in_step;
+      float acc = n < prm.N ? RD::partial(fp.O + head + (int64_t)n * prm.sn, fp.dO + head + (int64_t)n * prm.sn, sub)
+                            : 0.f;
+      acc = RD::reduce(acc);
+      if (sub == 0 && n < prm.N) fp.D[(int64_t)bh * prm.N + n] = acc;
+    }
+  }
+  if (zero) {
+    float4* z = reinterpret_cast<float4*>(prm.dq_accum + ((int64_t)bh * prm.n_tiles + tile) * kBlk * HD);
+    for (int k = threadIdx.x; k < kBlk * HD / 4; k += kThreads) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// P item: query tiles [item * kTilesPerItem, +kTilesPerItem) of head bh.
+template <int HD>
+__device__ __forceinline__ void pre_item(const BwdParams& prm, const FusedParams& fp, int bh, int item, bool zero) {
+  const int t1 = min(prm.n_tiles, (item + 1) * kTilesPerItem);
+  for (int tile = item * kTilesPerItem; tile < t1; ++tile) pre_tile<HD>(prm, fp, bh, tile, zero);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) atomicAdd(fp.sync + 1 + bh, 1);
+}
+
+// C item: dQ rows [tile * 128, +128) of head bh = bf16(scale * accumulator),
+// once every key block of the head is done; the tile goes through shared
+// memory to undo the unit-blocked layout.  Deterministic: the key blocks'
+// slices are summed in increasing order (causal: those that reach the tile).
+template <int HD, bool kDet>
+__device__ __forceinline__ void cvt_tile(const BwdParams& prm, const FusedParams& fp, uint8_t* smem, int bh,
+                                         int tile) {
+  constexpr int kPitch = HD + 4;
+  float* tile_s = reinterpret_cast<float*>(smem);
+  const float4* src = reinterpret_cast<const float4*>(prm.dq_accum + ((int64_t)bh * prm.n_tiles + tile) * kBlk * HD);
+  int last = 0;
+  if (kDet) {
+    last = prm.nk_tiles - 1;
+    if (prm.causal) {
+      const int64_t hi = (int64_t)tile * kBlk + kBlk - 1 + prm.offset;
+      last = hi < 0 ? -1 : (hi / kBlk < last ? (int)(hi / kBlk) : last);
+    }
+  }
+  const int64_t slice4 = prm.slice_elems / 4;
+  // a tile is 4 x (HD / 16) units of [4 column groups][32 rows][4 columns]
+  for (int k = threadIdx.x; k < kBlk * HD / 4; k += kThreads) {
+    const int unit = k / 128, g = (k % 128) / 32, r = k % 32;
+    const int row = (unit / (HD / 16)) * 32 + r, col = (unit % (HD / 16)) * 16 + g * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (last >= 0) v = __ldcg(src + k);
+    for (int sl = 1; sl <= last; ++sl) {
+      const float4 w = __ldcg(src + sl * slice4 + k);
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
+    }
+    *reinterpret_cast<float4*>(tile_s + row * kPitch + col) = v;
+  }
+  __syncthreads();
+  const int b = bh / prm.H, h = bh % prm.H;
+  __nv_bfloat16* out = fp.dQ + (int64_t)b * prm.sb + (int64_t)h * prm.sh;
+  constexpr int kPerRow = HD / 8;  // 16-byte stores per row
+  for (int k = threadIdx.x; k < kBlk * kPerRow; k += kThreads) {
+    const int r = k / kPerRow, c = (k % kPerRow) * 8;
+    const int n = tile * kBlk + r;
+    if (n >= prm.N) continue;
+    const float* v = tile_s + r * kPitch + c;
+    uint4 u;
+    u.x = ptx::pack_bf16x2(prm.scale * v[0], prm.scale * v[1]);
+    u.y = ptx::pack_bf16x2(prm.scale * v[2], prm.scale * v[3]);
+    u.z = ptx::pack_bf16x2(prm.scale * v[4], prm.scale * v[5]);
+    u.w = ptx::pack_bf16x2(prm.scale * v[6], prm.scale * v[7]);
+    *reinterpret_cast<uint4*>(out + (int64_t)n * prm.sn + c) = u;
+  }
+}
+
+// C item: query tiles [item * kTilesPerItem, +kTilesPerItem) of head bh, once
+// every key block of the head is done.
+template <int HD, bool kDet>
+__device__ __forceinline__ void cvt_item(const BwdParams& prm, const FusedParams& fp, uint8_t* smem, int bh,
+                                         int item) {
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + kBlk * (HD + 4) * 4);
+  const int BH = prm.B * prm.H;
+  if (threadIdx.x == 0) {
+    const bool ok = wait_counter(fp.sync + 1 + BH + bh, prm.nk_tiles, prm.wait_ns);
+    if (!ok) atomicCAS(prm.status, 0, (int32_t)FA_ERR_TIMEOUT);
+    *flag = ok;
+  }
+  __syncthreads();
+  if (!*flag) return;
+  const int t1 = min(prm.n_tiles, (item + 1) * kTilesPerItem);
+  for (int tile = item * kTilesPerItem; tile < t1; ++tile) {
+    cvt_tile<HD, kDet>(prm, fp, smem, bh, tile);
+    __syncthreads();  // the shared tile is rewritten by the next one
+  }
+}
+
+template <int HD, bool kDet, bool kRect>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const BwdParams prm, const FusedParams fp) {
+  using Ly = Layout<(HD <= 64 ? 64 : 128)>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  volatile int32_t* slot = reinterpret_cast<volatile int32_t*>(smem + Ly::kMisc + 8);
+  if (threadIdx.x == 0) *slot = atomicAdd(fp.sync, 1);
+  __syncthreads();
+  const int ticket = *slot;
+  __syncthreads();  // the slot's bytes are free again before any role uses shared memory
+  const int BH = prm.B * prm.H;
+  int role, bh, idx;
+  const int Ti = (prm.n_tiles + kTilesPerItem - 1) / kTilesPerItem;  // P and C items per head
+  fused_item(ticket, BH, Ti, prm.nk_tiles, role, bh, idx);
+  if (role == kItemBwd)
+    bwd_block<HD, kDet, kRect, true>(tmQ, tmK, tmV, tmdO, prm, idx, bh, fp.sync + 1 + bh, Ti,
+                                     fp.sync + 1 + BH + bh);
+  else if (role == kItemPre)
+    pre_item<HD>(prm, fp, bh, idx, !kDet);
+  else
+    cvt_item<HD, kDet>(prm, fp, smem, bh, idx);
 }
 
 template <int HD, bool kDet, bool kRect>
@@ -649,6 +919,28 @@ cudaError_t launch_d(const fa_problem& p, const CUtensorMap* maps, const BwdPara
                      cudaStream_t s) {
   if (det) return rect ? launch_hd<HD, true, true>(p, maps, prm, s) : launch_hd<HD, true, false>(p, maps, prm, s);
   return rect ? launch_hd<HD, false, true>(p, maps, prm, s) : launch_hd<HD, false, false>(p, maps, prm, s);
+}
+
+template <int HD, bool kDet, bool kRect>
+cudaError_t launch_fused_hd(const CUtensorMap* maps, const BwdParams& prm, const FusedParams& fp, int64_t items,
+                            cudaStream_t s) {
+  using Ly = Layout<(HD <= 64 ? 64 : 128)>;
+  cudaError_t e = cudaFuncSetAttribute(bwd_fused_kernel<HD, kDet, kRect>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  if (e != cudaSuccess) return e;
+  bwd_fused_kernel<HD, kDet, kRect><<<(unsigned)items, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                                prm, fp);
+  return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_fused_d(const CUtensorMap* maps, const BwdParams& prm, const FusedParams& fp, int64_t items,
+                           bool det, bool rect, cudaStream_t s) {
+  if (det)
+    return rect ? launch_fused_hd<HD, true, true>(maps, prm, fp, items, s)
+                : launch_fused_hd<HD, true, false>(maps, prm, fp, items, s);
+  return rect ? launch_fused_hd<HD, false, true>(maps, prm, fp, items, s)
+              : launch_fused_hd<HD, false, false>(maps, prm, fp, items, s);
 }
 
 }  // namespace
@@ -688,13 +980,10 @@ bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p, b
   return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
-                             const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
-                             uint64_t wait_ns, cudaStream_t s) {
-  CUtensorMap maps[4];
-  if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
-      !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false))
-    return cudaErrorInvalidValue;
+namespace {
+// Kernel parameters shared by the separate and the single-launch backward.
+BwdParams bwd_params(const fa_problem& p, const float* L, const float* D, float* dq_accum, void* dK, void* dV,
+                     int32_t* status, uint64_t wait_ns) {
   BwdParams prm;
   prm.L = L;
   prm.D = D;
@@ -719,6 +1008,18 @@ cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, 
   prm.scale = p.scale;
   prm.causal = p.causal;
   prm.slice_elems = deterministic(p) ? dq_slice_elems(p) : 0;
+  return prm;
+}
+}  // namespace
+
+cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
+                             const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
+                             uint64_t wait_ns, cudaStream_t s) {
+  CUtensorMap maps[4];
+  if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
+      !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false))
+    return cudaErrorInvalidValue;
+  BwdParams prm = bwd_params(p, L, D, dq_accum, dK, dV, status, wait_ns);
   const bool det = prm.slice_elems > 0;
   const bool rect = p.causal && prm.offset != 0;
   switch (p.d) {
@@ -726,6 +1027,39 @@ cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, 
     case 64: return launch_d<64>(p, maps, prm, det, rect, s);
     case 96: return launch_d<96>(p, maps, prm, det, rect, s);
     case 128: return launch_d<128>(p, maps, prm, det, rect, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int64_t fused_items(const fa_problem& p) {
+  return (int64_t)p.B * p.H * (2 * ceil_div(ceil_div(p.N, kBlk), kTilesPerItem) + ceil_div(p.N_k, kBlk));
+}
+
+cudaError_t launch_bwd_fused_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* O,
+                                   const void* dO, const float* L, float* D, float* dq_accum, int32_t* sync, void* dQ,
+                                   void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s) {
+  const int64_t items = fused_items(p);
+  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  CUtensorMap maps[4];
+  if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
+      !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false))
+    return cudaErrorInvalidValue;
+  const BwdParams prm = bwd_params(p, L, D, dq_accum, dK, dV, status, wait_ns);
+  FusedParams fp;
+  fp.O = (const __nv_bfloat16*)O;
+  fp.dO = (const __nv_bfloat16*)dO;
+  fp.dQ = (__nv_bfloat16*)dQ;
+  fp.D = D;
+  fp.sync = sync;
+  cudaError_t e = cudaMemsetAsync(sync, 0, sizeof(int32_t) * (1 + 2 * (size_t)p.B * p.H), s);
+  if (e != cudaSuccess) return e;
+  const bool det = prm.slice_elems > 0;
+  const bool rect = p.causal && prm.offset != 0;
+  switch (p.d) {
+    case 32: return launch_fused_d<32>(maps, prm, fp, items, det, rect, s);
+    case 64: return launch_fused_d<64>(maps, prm, fp, items, det, rect, s);
+    case 96: return launch_fused_d<96>(maps, prm, fp, items, det, rect, s);
+    case 128: return launch_fused_d<128>(maps, prm, fp, items, det, rect, s);
   }
   return cudaErrorInvalidValue;
 }

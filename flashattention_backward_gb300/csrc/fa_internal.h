@@ -68,6 +68,13 @@ cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, c
 cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V,
                              const void* dO, const float* L, const float* D, float* dq_accum,
                              void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
+// The whole backward (preprocess, tcgen05 backward, convert) in one launch
+// of the tcgen05 kernel for bf16, d in {32, 64, 96, 128}; sync holds
+// 1 + 2 B H int32 (zeroed by the launcher).
+int64_t fused_items(const fa_problem& p);
+cudaError_t launch_bwd_fused_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* O,
+                                   const void* dO, const float* L, float* D, float* dq_accum, int32_t* sync,
+                                   void* dQ, void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
 // tcgen05 forward for bf16, d in {32, 64, 96, 128}.
 cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                              int32_t* status, uint64_t wait_ns, cudaStream_t s);

@@ -169,6 +169,26 @@ fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const v
                       const void* O, const void* dO, const float* L, float* D,
                       float* dQ_accum, void* dQ, void* dK, void* dV, void* stream);
 
+/* The same backward as fa_backward in one kernel launch: the preprocess
+ * (ch.16 §16.8 item 1), the main kernel and the convert (§16.3) as items of
+ * one grid; the pages launch them separately.  Each CTA of the grid takes a
+ * ticket in the order CTAs
+ * start and the ticket names its item: one query tile's D and zeroed
+ * accumulator tile, one key block of the backward, or one query tile's
+ * conversion.  Items only wait (bounded) for items with smaller tickets, so
+ * the preprocess of the next group of heads and the conversion of the
+ * previous one overlap the backward of the current one.  Only problems that
+ * run on the tensor-core kernels (bf16, d <= 128); others return
+ * FA_ERR_UNSUPPORTED.  D and dQ_accum as for fa_backward; sync: device
+ * int32 array of fa_backward_fused_sync_elems(p) elements, scratch owned by
+ * the caller (zeroed on `stream` before the launch).  Same results as
+ * fa_backward (bitwise with FA_FLAG_DETERMINISTIC). */
+size_t fa_backward_fused_sync_elems(const fa_problem* p);
+fa_status fa_backward_fused(const fa_problem* p, const void* Q, const void* K, const void* V,
+                            const void* O, const void* dO, const float* L, float* D,
+                            float* dQ_accum, int32_t* sync, void* dQ, void* dK, void* dV,
+                            void* stream);
+
 /* Backward pass for tensors in host memory (page-locked for overlap):
  * Q, O, dO, dQ dense [B, H, N, d] and K, V, dK, dV dense [B, H, N_k, d] host
  * arrays (p's strides must say so: stride_n = d, stride_h = rows*d,

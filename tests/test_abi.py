@@ -113,6 +113,22 @@ def test_validation_rejects(lib, kw, code):
     assert r == code
 
 
+def test_fused_backward_host_checks(lib):
+    p = _prob(B=2, H=3)
+    assert lib.fa_backward_fused_sync_elems(ctypes.byref(p)) == 1 + 2 * 6
+    p32 = _prob(dtype=fa.FA_FP32, stride_b=2 * 100 * 64, stride_h=100 * 64, stride_n=64)
+    assert lib.fa_backward_fused_sync_elems(ctypes.byref(p32)) == 0  # CUDA-core problems: separate launches only
+    args = [BAD] * 13
+    assert lib.fa_backward_fused(ctypes.byref(p32), *args, None) == fa.FA_ERR_UNSUPPORTED
+    p256 = _prob(d=256, stride_b=2 * 100 * 256, stride_h=100 * 256, stride_n=256)
+    assert lib.fa_backward_fused(ctypes.byref(p256), *args, None) == fa.FA_ERR_UNSUPPORTED
+    bad_sync = list(args)
+    bad_sync[9] = BAD + 2  # sync must be 4-byte aligned
+    assert lib.fa_backward_fused(ctypes.byref(p), *bad_sync, None) == fa.FA_ERR_INVALID_ARG
+    bad_sync[9] = 0
+    assert lib.fa_backward_fused(ctypes.byref(p), *bad_sync, None) == fa.FA_ERR_INVALID_ARG
+
+
 def test_null_and_misaligned_pointers(lib):
     p = _prob()
     assert lib.fa_bwd(None, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, BAD, None) == fa.FA_ERR_INVALID_ARG
