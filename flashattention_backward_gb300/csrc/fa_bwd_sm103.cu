@@ -84,12 +84,12 @@ enum BarId {
   DOEMPTY0,     // dO stage free again
   DOEMPTY1,
   S_FULL,       // S^T(i) in TMEM
-  P_FULL,       // P^T(i) in TMEM (256 arrivals)
+  P_FULL,       // P^T(i) in TMEM (one per compute thread)
   DV_DONE,      // dV(i) product done: S/P columns reusable
   DP_FULL,      // dP^T(i) in TMEM
-  DS_FULL,      // dS^T(i) in shared memory (256 arrivals)
-  DQ_FULL,      // dQ(i) in TMEM; dS(i) and Q(i) consumed
-  DQ_EMPTY,     // dQ(i) drained from TMEM (256 arrivals)
+  DS_FULL,      // dS^T(i) in shared memory (one per compute thread)
+  DQ_FULL,      // dQ(i) in TMEM
+  DQ_EMPTY,     // dQ(i) drained from TMEM (one per compute thread)
   ACC_FULL,     // every MMA done: dK, dV final
   kNumBars
 };
@@ -397,8 +397,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       const uint32_t ph = i & 1;
       // dV += P^T dO   (A = P^T from TMEM: the 16-query k-steps 2g, 2g+1 in
       // columns [32g, 32g + 16))
-      if (!(ok = warp_wait(bar(P_FULL), ph, W))) break;
-      if (!(ok = warp_wait(bar(DOFULL0 + sd), (i / kDoSt) & 1, W))) break;
+      if (!(ok = warp_wait2(bar(P_FULL), ph, bar(DOFULL0 + sd), (i / kDoSt) & 1, W))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
 #pragma unroll
@@ -421,22 +420,23 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       __syncwarp();
       // S^T(i+1) = K Q(i+1)^T once dV(i) has read P(i)
       if (i + 1 < n_iter) {
-        if (!(ok = warp_wait(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W))) break;
-        if (!(ok = warp_wait(bar(DV_DONE), ph, W))) break;
+        if (!(ok = warp_wait2(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, bar(DV_DONE), ph, W))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) issue_S(st ^ 1);
         __syncwarp();
       }
-      // dK += dS^T Q ;  dQ = dS K
+      // dQ = dS K ;  dK += dS^T Q.  dQ first: its drain overlaps dK.  The
+      // compute warps overwrite dS only after DP_FULL of the next block,
+      // which completes after this dK.
       if (!(ok = warp_wait(bar(DS_FULL), ph, W))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          ptx::mma_ss(tdK, kdesc(sdS, kk), mndesc(sQ(st), kk), kIdKV, (i | kk) != 0);
-#pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk) ptx::mma_ss(tdQ, mndesc(sdS, kk), mndesc(sK, kk), kIdQ, kk > 0);
         ptx::tc_commit(bar(DQ_FULL));
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)
+          ptx::mma_ss(tdK, kdesc(sdS, kk), mndesc(sQ(st), kk), kIdKV, (i | kk) != 0);
         ptx::tc_commit(bar(QEMPTY0 + st));
       }
       __syncwarp();
@@ -592,7 +592,8 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         issue_reds(Hi{});
         pending_hi = false;
       }
-      // ---- dQ(i-1); also guarantees dS(i-1) has been consumed
+      // ---- dQ(i-1).  dS(i) is written after DP_FULL(i), which completes
+      // after dK(i-1), the last reader of dS(i-1).
       if (i > 0 && !(ok = drain_dq(i - 1))) break;
       // ---- dS(i)
       if (!(ok = warp_wait(bar(DP_FULL), ph, W))) break;
