@@ -195,7 +195,7 @@ fa_status fa_backward_fused(const fa_problem* p, const void* Q, const void* K, c
  * stride_b = H*rows*d), L a dense [B, H, N] float32 host array.
  * Heads are independent, so the batch streams through `workspace` (device
  * memory, 256-byte aligned, at least fa_backward_host_workspace_bytes()) in
- * groups of `heads_per_group` heads (0: about four groups): group c+1 is
+ * groups of `heads_per_group` heads (0: about eight groups): group c+1 is
  * copied in and group c-1 copied out while group c runs fa_backward on
  * `stream`.  Returns after enqueueing; `stream` continues only once the last
  * result has reached host memory.  Copies use two library-owned streams
