@@ -38,9 +38,10 @@
 //               for d <= 64, else 128)
 //
 // MMA issue order per query block i (software pipelined):
-//   dV(i)  dP(i)  S(i+1)  dK(i)  dQ(i)
+//   dV(i)  dP(i)  S(i+1)  dQ(i)  dK(i)
 // so the tensor pipe works on S(i+1) while the compute warps turn dP(i) into
-// dS(i), and on dK(i), dQ(i), dV(i+1) while they turn S(i+1) into P(i+1).
+// dS(i), and on dQ(i), dK(i), dV(i+1) while they turn S(i+1) into P(i+1);
+// dQ goes first so that its drain overlaps dK.
 //
 // Every wait is bounded; when one runs out the CTA records FA_ERR_TIMEOUT,
 // drains its own TMA loads, MMAs and bulk reductions, frees tensor memory and
