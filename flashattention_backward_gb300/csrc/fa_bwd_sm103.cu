@@ -14,21 +14,20 @@
 // what dV += P^T dO and dK += dS^T Q need, and P^T feeds the dV product
 // straight from tensor memory.
 //
-// Warp roles (576 threads):
+// Warp roles (704 threads):
 //   warps 0-15 compute.  Warp w owns TMEM lanes 32*(w%4) .. +31 (key rows for
-//              S, dP, dV, dK; query rows for dQ) and column quarter w/4 of
-//              them (four warps per SM sub-partition hide each other's
-//              latencies).
+//              S, dP, dV, dK) and column quarter w/4 of them (four warps per
+//              SM sub-partition hide each other's latencies).
 //              Per query block: P = exp2(S*scale*log2e - L*log2e) -> bf16
-//              into TMEM; dQ of the previous block TMEM -> registers ->
-//              fp32 reductions into global (a bulk reduction staged through
-//              shared memory where it has room, else vector reductions from
-//              registers); dS = P * (dP - D) -> bf16
-//              into shared memory (128-byte swizzle).  Epilogue: dV (w < 8)
-//              and scale * dK (w >= 8), half the columns each.
-//   warp 16    TMA producer: K, V once; Q (two stages, with its L and D rows)
+//              into TMEM; dS = P * (dP - D) -> bf16 into shared memory
+//              (128-byte swizzle).  Epilogue: dV (w < 8) and scale * dK
+//              (w >= 8), half the columns each.
+//   warps 16-19 dQ drain, one per TMEM lane quarter (query rows of dQ):
+//              TMEM -> shared memory -> bulk fp32 reductions into the
+//              accumulator, off the compute warps' path.
+//   warp 20    TMA producer: K, V once; Q (two stages, with its L and D rows)
 //              and dO (one stage for d = 128, two for d = 64).
-//   warp 17    TMEM allocator and MMA issuer (one elected lane issues).
+//   warp 21    TMEM allocator and MMA issuer (one elected lane issues).
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128)     S^T; P^T (bf16) is written over it: query columns
@@ -38,10 +37,11 @@
 //               for d <= 64, else 128)
 //
 // MMA issue order per query block i (software pipelined):
-//   dV(i)  dP(i)  S(i+1)  dQ(i)  dK(i)
-// so the tensor pipe works on S(i+1) while the compute warps turn dP(i) into
-// dS(i), and on dQ(i), dK(i), dV(i+1) while they turn S(i+1) into P(i+1);
-// dQ goes first so that its drain overlaps dK.
+//   dV(i)  S(i+1)  dQ(i)  dK(i)  dP(i+1)
+// dQ goes first so that its drain starts early, and dP(i+1) is issued as soon
+// as the drain warps have read dQ(i) out of the columns dP shares, so the
+// tensor pipe computes dP(i+1) while the compute warps turn S(i+1) into
+// P(i+1).
 //
 // Every wait is bounded; when one runs out the CTA records FA_ERR_TIMEOUT,
 // drains its own TMA loads, MMAs and bulk reductions, frees tensor memory and
@@ -66,11 +66,15 @@ namespace fa {
 namespace {
 
 constexpr int kBlk = 128;  // Br = Bc = 128
-constexpr int kComputeWarps = 16;           // 4 per TMEM lane quarter
-constexpr int kProducerWarp = kComputeWarps;
-constexpr int kMmaWarp = kComputeWarps + 1;  // on the same SM sub-partition as lane quarter 1
-constexpr int kThreads = 32 * (kComputeWarps + 2);
+constexpr int kComputeWarps = 16;               // 4 per TMEM lane quarter
+constexpr int kDrainWarps = 4;                  // 1 per TMEM lane quarter
+constexpr int kDrainWarp0 = kComputeWarps;      // warps 16-19
+constexpr int kProducerWarp = kComputeWarps + kDrainWarps;
+constexpr int kMmaWarp = kProducerWarp + 1;     // on the same SM sub-partition as lane quarter 1
+constexpr int kThreads = 32 * (kComputeWarps + kDrainWarps + 2);
 constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kDrainThreads = 32 * kDrainWarps;
+constexpr int kStagedUnits = 4;                 // dQ units per drain warp staged for one bulk reduction
 constexpr int kHeadGroup = 4;  // heads whose key blocks interleave in the grid order
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -90,7 +94,7 @@ enum BarId {
   DP_FULL,      // dP^T(i) in TMEM
   DS_FULL,      // dS^T(i) in shared memory (one per compute thread)
   DQ_FULL,      // dQ(i) in TMEM
-  DQ_EMPTY,     // dQ(i) drained from TMEM (one per compute thread)
+  DQ_EMPTY,     // dQ(i) drained from TMEM (one per drain thread)
   ACC_FULL,     // every MMA done: dK, dV final
   kNumBars
 };
@@ -108,10 +112,10 @@ struct Layout {
   static constexpr int kQ = kV + kTile;                 // 2 stages
   static constexpr int kdO = kQ + 2 * kTile;            // kDoStages stages
   static constexpr int kdS = kdO + kDoStages * kTile;   // 128 x 128 bf16, two 64-column chunks
-  // dQ staging for bulk reductions: lane quarters 0 and 1, one slot of
-  // 32 x LD/4 fp32 per warp
+  // dQ staging for bulk reductions: one slot of kStagedUnits 2 KB units
+  // (32 rows x 16 fp32 columns each) per drain warp
   static constexpr int kStage = kdS + 2 * kChunk;
-  static constexpr int kStageBytes = 8 * 32 * (LD / 4) * 4;
+  static constexpr int kStageBytes = kDrainWarps * kStagedUnits * 2048;
   static constexpr int kL = kStage + kStageBytes;      // 2 stages x 128 fp32 (L * log2 e)
   static constexpr int kD = kL + 2 * kBlk * 4;          // 2 stages x 128 fp32
   static constexpr int kBar = kD + 2 * kBlk * 4;
@@ -241,7 +245,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     ptx::mbar_init(bar(DP_FULL), 1);
     ptx::mbar_init(bar(DS_FULL), kComputeThreads);
     ptx::mbar_init(bar(DQ_FULL), 1);
-    ptx::mbar_init(bar(DQ_EMPTY), kComputeThreads);
+    ptx::mbar_init(bar(DQ_EMPTY), kDrainThreads);
     ptx::mbar_init(bar(ACC_FULL), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -386,10 +390,22 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       ptx::tc_commit(bar(S_FULL));
     };
 
-    bool ok = warp_wait(bar(KV_FULL), 0, W) && warp_wait(bar(QFULL0), 0, W);
+    // dP^T = V dO^T into the columns that held dQ of the previous block
+    auto issue_dP = [&](int sd) {
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tdP, kdesc(sV, kk), kdesc(sdO(sd), kk), kIdS, kk > 0);
+      ptx::tc_commit(bar(DP_FULL));
+    };
+
+    // Per query block i: dV(i), S(i+1), dQ(i), dK(i), then dP(i+1) as soon
+    // as the drain warps have read dQ(i) out of the columns dP shares.
+    bool ok = warp_wait(bar(KV_FULL), 0, W) && warp_wait2(bar(QFULL0), 0, bar(DOFULL0), 0, W);
     if (ok) {
       ptx::tc_fence_after();
-      if (ptx::elect_one()) issue_S(0);
+      if (ptx::elect_one()) {
+        issue_S(0);
+        issue_dP(0);
+      }
       __syncwarp();
     }
     for (int i = 0; ok && i < n_iter; ++i) {
@@ -397,25 +413,14 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       const int sd = i % kDoSt;
       const uint32_t ph = i & 1;
       // dV += P^T dO   (A = P^T from TMEM: the 16-query k-steps 2g, 2g+1 in
-      // columns [32g, 32g + 16))
-      if (!(ok = warp_wait2(bar(P_FULL), ph, bar(DOFULL0 + sd), (i / kDoSt) & 1, W))) break;
+      // columns [32g, 32g + 16)); dO(i) is free once this has read it
+      if (!(ok = warp_wait(bar(P_FULL), ph, W))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
           ptx::mma_ts(tdV, tS + (kk >> 1) * 32 + (kk & 1) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
         ptx::tc_commit(bar(DV_DONE));
-      }
-      __syncwarp();
-      // dP^T = V dO^T  (its columns held dQ(i-1): wait until drained)
-      if (i > 0) {
-        if (!(ok = warp_wait(bar(DQ_EMPTY), (i - 1) & 1, W))) break;
-        ptx::tc_fence_after();
-      }
-      if (ptx::elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tdP, kdesc(sV, kk), kdesc(sdO(sd), kk), kIdS, kk > 0);
-        ptx::tc_commit(bar(DP_FULL));
         ptx::tc_commit(bar(DOEMPTY0 + sd));
       }
       __syncwarp();
@@ -426,7 +431,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         if (ptx::elect_one()) issue_S(st ^ 1);
         __syncwarp();
       }
-      // dQ = dS K ;  dK += dS^T Q.  dQ first: its drain overlaps dK.  The
+      // dQ = dS K ;  dK += dS^T Q.  dQ first so the drain starts early.  The
       // compute warps overwrite dS only after DP_FULL of the next block,
       // which completes after this dK.
       if (!(ok = warp_wait(bar(DS_FULL), ph, W))) break;
@@ -441,10 +446,100 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         ptx::tc_commit(bar(QEMPTY0 + st));
       }
       __syncwarp();
+      // dP(i+1) once dQ(i) has been drained and dO(i+1) has landed
+      if (i + 1 < n_iter) {
+        const int sd1 = (i + 1) % kDoSt;
+        if (!(ok = warp_wait2(bar(DQ_EMPTY), ph, bar(DOFULL0 + sd1), ((i + 1) / kDoSt) & 1, W))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) issue_dP(sd1);
+        __syncwarp();
+      }
     }
     if (ptx::elect_one()) ptx::tc_commit(bar(ACC_FULL));
     __syncwarp();
     if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
+  } else if (warp >= kDrainWarp0) {
+    // ------------------------------------------------------------ dQ drain
+    // One warp per TMEM lane quarter reads its 32 query rows of dQ(i) out of
+    // tensor memory as soon as the MMA has produced them, frees the columns
+    // for dP(i+1), then adds them to the fp32 accumulator as bulk reductions
+    // by the TMA unit, staged through this warp's slot of kStagedUnits 2 KB
+    // units: the first units straight from the tensor-memory loads, the rest
+    // (d > 64) from registers once the first operation has read the slot.
+    // Vector reductions from registers would queue in the sub-partition's
+    // memory pipe ahead of the compute warps' shared-memory traffic (18 %
+    // slower at d = 128, measured).  The compute warps never wait for this.
+    const int qq = warp & 3;
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    constexpr int kUnitsQ = HD / 16;                      // 16-column units of this lane quarter
+    constexpr int kStaged = kUnitsQ < kStagedUnits ? kUnitsQ : kStagedUnits;
+    constexpr int kHeld = kUnitsQ - kStaged;              // units held in registers for a second round
+    constexpr bool det = kDet;                            // store into this key block's slice instead of adding
+    const uint32_t slot = sbase + Ly::kStage + qq * (kStagedUnits * 2048);
+    bool ok = true;
+    for (int i = 0; i < n_iter; ++i) {
+      if (!(ok = warp_wait(bar(DQ_FULL), i & 1, W))) break;
+      ptx::tc_fence_after();
+      float* dst = prm.dq_accum + (det ? kb * prm.slice_elems : 0) +
+                   dq_unit_offset(bh, prm.n_tiles, q_first + i, qq, 0, HD);
+      if (lane == 0) ptx::bulk_wait_read_all();
+      __syncwarp();
+      // staged units, 32 columns (two units) per TMEM load
+#pragma unroll
+      for (int u = 0; u < kStaged; u += 2) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + u * 16, r);
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            ptx::st_shared_v4(slot + (u + v) * 2048 + g * 512 + lane * 16, r[v * 16 + 4 * g], r[v * 16 + 4 * g + 1],
+                              r[v * 16 + 4 * g + 2], r[v * 16 + 4 * g + 3]);
+      }
+      uint32_t h[kHeld > 0 ? kHeld * 16 : 1];
+      if constexpr (kHeld == 4) {
+        ptx::tmem_ld64(tm + Ly::kColdQ + lane_off + kStaged * 16, tm + Ly::kColdQ + lane_off + kStaged * 16 + 32,
+                       *reinterpret_cast<uint32_t(*)[64]>(h));
+      } else if constexpr (kHeld == 2) {
+        ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + kStaged * 16, *reinterpret_cast<uint32_t(*)[32]>(h));
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(DQ_EMPTY));  // the columns are free for dP(i+1)
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (det)
+          ptx::bulk_store(dst, slot, kStaged * 2048);
+        else
+          ptx::bulk_reduce_add_f32(dst, slot, kStaged * 2048);
+        ptx::bulk_commit();
+      }
+      if constexpr (kHeld > 0) {
+        // second round through the same slot once the first has been read
+        if (lane == 0) ptx::bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < kHeld; ++u)
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            ptx::st_shared_v4(slot + u * 2048 + g * 512 + lane * 16, h[u * 16 + 4 * g], h[u * 16 + 4 * g + 1],
+                              h[u * 16 + 4 * g + 2], h[u * 16 + 4 * g + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (det)
+            ptx::bulk_store(dst + kStaged * kDqUnitFloats, slot, kHeld * 2048);
+          else
+            ptx::bulk_reduce_add_f32(dst + kStaged * kDqUnitFloats, slot, kHeld * 2048);
+          ptx::bulk_commit();
+        }
+      }
+    }
+    if (lane == 0) {
+      ptx::bulk_wait_all();  // this warp's bulk operations are complete
+      if (kFused) asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ compute
     const int qq = warp & 3;               // TMEM lane quarter
@@ -456,93 +551,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     const int kd = kRect ? k0 - prm.offset : k0;  // key k0 + t visible to query q iff q - kd >= t
     const float sl2 = prm.scale * kLog2e;
     const int c0 = G * 32;                 // query columns [c0, c0 + 32) of S, dP
-    // this warp's dQ columns [G * kCols, +kCols): d = 128, 64 all four
-    // column quarters; d = 96 (32) only the first three (two)
-    constexpr int kCols = LD / 4;
-    constexpr int kUnits = kCols / 16;     // 2 KB units, contiguous in the accumulator
-    const bool dq_cols = HD == LD || G * kCols < HD;
-    constexpr int kRedsHalf = kCols / 8;   // 16-byte reductions per lane per query block, halved
-    // Vector reductions from registers queue in the SM sub-partition's memory
-    // pipe ahead of the warp's own shared-memory loads, barrier waits and
-    // arrivals (and, on lane quarter 1, delay the MMA warp's tcgen05.mma
-    // issue).  So the warps of lane quarters 0 and 1 (as many as the shared
-    // memory left at d = 128 holds) stage their dQ share there and hand it
-    // to the TMA unit as one bulk reduction, one slot per warp: the operation
-    // issued one query block earlier has long read it.  The other warps issue
-    // vector reductions: at d = 128 in two halves, each right after the warp
-    // has signalled its next dS and P results; at d = 64 (half the work per
-    // block) right after the drain, while the warps wait for dV and dP.
-    constexpr bool kSplit = LD == 128;
-    const bool staged = qq <= 1 && dq_cols;
-    constexpr bool det = kDet;             // store into this key block's slice instead of adding
-    int rounds = 0;                        // bulk operations issued by this warp
     uint32_t pk[16];                       // P for columns c0 .. c0 + 31, bf16 pairs
-    uint32_t dq[kCols];                    // drained dQ of the previous query block
-    bool pending_lo = false, pending_hi = false;
-    float* dq_dst = nullptr;               // its first unit in the accumulator
-
-    auto issue_reds = [&](auto m0c) {      // 16-byte pieces m0 .. m0 + kRedsHalf - 1 of dq
-      constexpr int m0 = decltype(m0c)::value;
-#pragma unroll
-      for (int m = m0; m < m0 + kRedsHalf; ++m) {
-        float* a = dq_dst + (m / 4) * kDqUnitFloats + (m % 4) * 128 + lane * 4;
-        if (det)
-          ptx::st_global_v4(a, __uint_as_float(dq[4 * m]), __uint_as_float(dq[4 * m + 1]),
-                            __uint_as_float(dq[4 * m + 2]), __uint_as_float(dq[4 * m + 3]));
-        else
-          ptx::red_add_v4(a, __uint_as_float(dq[4 * m]), __uint_as_float(dq[4 * m + 1]),
-                          __uint_as_float(dq[4 * m + 2]), __uint_as_float(dq[4 * m + 3]));
-      }
-    };
-    using Lo = std::integral_constant<int, 0>;
-    using Hi = std::integral_constant<int, kRedsHalf>;
-
-    // dQ(it): TMEM -> registers, then the TMEM columns are released.
-    auto drain_dq = [&](int it) -> bool {
-      if (!warp_wait(bar(DQ_FULL), it & 1, W)) return false;
-      ptx::tc_fence_after();
-      if (dq_cols) {
-        if constexpr (kCols == 32) {
-          ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + G * 32, *reinterpret_cast<uint32_t(*)[32]>(dq));
-        } else {
-          ptx::tmem_ld16(tm + Ly::kColdQ + lane_off + G * 16, *reinterpret_cast<uint32_t(*)[16]>(dq));
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(DQ_EMPTY));
-      if (!dq_cols) return true;
-      dq_dst = prm.dq_accum + (det ? kb * prm.slice_elems : 0) +
-               dq_unit_offset(bh, prm.n_tiles, q_first + it, qq, G * kUnits, HD);
-      if (staged) {
-        // one slot per warp, free once the operation issued one query block
-        // earlier has read it
-        const uint32_t buf = sbase + Ly::kStage + (qq * 4 + G) * (kUnits * 2048);
-        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < kUnits; ++u)
-#pragma unroll
-          for (int g = 0; g < 4; ++g)
-            ptx::st_shared_v4(buf + u * 2048 + g * 512 + lane * 16, dq[u * 16 + 4 * g], dq[u * 16 + 4 * g + 1],
-                              dq[u * 16 + 4 * g + 2], dq[u * 16 + 4 * g + 3]);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (det)
-            ptx::bulk_store(dq_dst, buf, kUnits * 2048);
-          else
-            ptx::bulk_reduce_add_f32(dq_dst, buf, kUnits * 2048);
-          ptx::bulk_commit();
-        }
-        ++rounds;
-      } else if (kSplit) {
-        pending_lo = pending_hi = true;
-      } else {
-        issue_reds(Lo{});
-        issue_reds(Hi{});
-      }
-      return true;
-    };
 
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
@@ -589,14 +598,8 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(P_FULL));
-      if (pending_hi) {
-        issue_reds(Hi{});
-        pending_hi = false;
-      }
-      // ---- dQ(i-1).  dS(i) is written after DP_FULL(i), which completes
-      // after dK(i-1), the last reader of dS(i-1).
-      if (i > 0 && !(ok = drain_dq(i - 1))) break;
-      // ---- dS(i)
+      // ---- dS(i).  Written after DP_FULL(i), which completes after dK(i-1),
+      // the last reader of dS(i-1).
       if (!(ok = warp_wait(bar(DP_FULL), ph, W))) break;
       ptx::tc_fence_after();
       {
@@ -627,23 +630,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(DS_FULL));
-      if (pending_lo) {
-        issue_reds(Lo{});
-        pending_lo = false;
-      }
     }
-    if (ok && pending_hi) issue_reds(Hi{});
-    pending_hi = false;
-    if (ok && n_iter > 0) ok = drain_dq(n_iter - 1);
-    if (ok && pending_lo) {
-      issue_reds(Lo{});
-      issue_reds(Hi{});
-    }
-    if (lane == 0) {
-      ptx::bulk_wait_all();  // this warp's bulk operations are complete
-      if (kFused) asm volatile("fence.proxy.async.global;" ::: "memory");
-    }
-    __syncwarp();
     if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
       ptx::tc_fence_after();
       constexpr int kHalf = HD / 2;        // warps G = 0, 1 store dV, G = 2, 3 store dK
