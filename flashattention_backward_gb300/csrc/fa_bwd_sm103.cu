@@ -88,7 +88,8 @@ enum BarId {
   DOFULL1,
   DOEMPTY0,     // dO stage free again
   DOEMPTY1,
-  S_FULL,       // S^T(i) in TMEM
+  S_FULL0,      // S^T(i) in TMEM buffer i % kSBufs (one barrier per buffer)
+  S_FULL1,
   P_FULL,       // P^T(i) in TMEM (one per compute thread)
   DV_DONE,      // dV(i) product done: S/P columns reusable
   DP_FULL,      // dP^T(i) in TMEM
@@ -121,7 +122,10 @@ struct Layout {
   static constexpr int kBar = kD + 2 * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
   static constexpr int kBytes = kMisc + 16;
-  static constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 128;
+  // S^T buffers: two where the accumulators leave room (LD = 64), so that
+  // S(i+1) need not wait for dV(i) to read P(i)
+  static constexpr int kSBufs = LD == 64 ? 2 : 1;
+  static constexpr uint32_t kColS = 0, kColS1 = 384, kColdP = 128, kColdQ = 128;
   static constexpr uint32_t kColdV = 256, kColdK = 256 + LD;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -239,7 +243,8 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     ptx::mbar_init(bar(DOFULL1), 1);
     ptx::mbar_init(bar(DOEMPTY0), 1);
     ptx::mbar_init(bar(DOEMPTY1), 1);
-    ptx::mbar_init(bar(S_FULL), 1);
+    ptx::mbar_init(bar(S_FULL0), 1);
+    ptx::mbar_init(bar(S_FULL1), 1);
     ptx::mbar_init(bar(P_FULL), kComputeThreads);
     ptx::mbar_init(bar(DV_DONE), 1);
     ptx::mbar_init(bar(DP_FULL), 1);
@@ -382,12 +387,15 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     auto mndesc = [&](uint32_t tile, int kk) -> uint64_t {
       return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
     };
-    const uint32_t tS = tm + Ly::kColS, tdP = tm + Ly::kColdP;
+    constexpr int kSB = Ly::kSBufs;
+    const uint32_t tdP = tm + Ly::kColdP;
     const uint32_t tdQ = tm + Ly::kColdQ, tdV = tm + Ly::kColdV, tdK = tm + Ly::kColdK;
-    auto issue_S = [&](int st) {
+    auto tS = [&](int i) -> uint32_t { return tm + (kSB == 2 && (i & 1) ? Ly::kColS1 : Ly::kColS); };
+    // S^T(i) = K Q(i)^T into buffer i % kSB
+    auto issue_S = [&](int i) {
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS, kdesc(sK, kk), kdesc(sQ(st), kk), kIdS, kk > 0);
-      ptx::tc_commit(bar(S_FULL));
+      for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS(i), kdesc(sK, kk), kdesc(sQ(i & 1), kk), kIdS, kk > 0);
+      ptx::tc_commit(bar(S_FULL0 + (kSB == 2 ? (i & 1) : 0)));
     };
 
     // dP^T = V dO^T into the columns that held dQ of the previous block
@@ -413,22 +421,28 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       const int sd = i % kDoSt;
       const uint32_t ph = i & 1;
       // dV += P^T dO   (A = P^T from TMEM: the 16-query k-steps 2g, 2g+1 in
-      // columns [32g, 32g + 16)); dO(i) is free once this has read it
-      if (!(ok = warp_wait(bar(P_FULL), ph, W))) break;
+      // columns [32g, 32g + 16)); dO(i) is free once this has read it.  With
+      // two S buffers dV(i-1) is also confirmed here (before DV_DONE(i) is
+      // committed), freeing the buffer S(i+1) goes into.
+      ok = kSB == 2 && i > 0 ? warp_wait2(bar(P_FULL), ph, bar(DV_DONE), ph ^ 1, W) : warp_wait(bar(P_FULL), ph, W);
+      if (!ok) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
-          ptx::mma_ts(tdV, tS + (kk >> 1) * 32 + (kk & 1) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
+          ptx::mma_ts(tdV, tS(i) + (kk >> 1) * 32 + (kk & 1) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
         ptx::tc_commit(bar(DV_DONE));
         ptx::tc_commit(bar(DOEMPTY0 + sd));
       }
       __syncwarp();
-      // S^T(i+1) = K Q(i+1)^T once dV(i) has read P(i)
+      // S^T(i+1) = K Q(i+1)^T once its buffer's last reader is done: dV(i)
+      // with one buffer, dV(i-1) (confirmed above) with two
       if (i + 1 < n_iter) {
-        if (!(ok = warp_wait2(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, bar(DV_DONE), ph, W))) break;
+        ok = kSB == 2 ? warp_wait(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W)
+                      : warp_wait2(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, bar(DV_DONE), ph, W);
+        if (!ok) break;
         ptx::tc_fence_after();
-        if (ptx::elect_one()) issue_S(st ^ 1);
+        if (ptx::elect_one()) issue_S(i + 1);
         __syncwarp();
       }
       // dQ = dS K ;  dK += dS^T Q.  dQ first so the drain starts early.  The
@@ -559,11 +573,15 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       const uint32_t ph = i & 1;
       const int q0 = (q_first + i) * kBlk;
       // ---- P(i)
-      if (!(ok = warp_wait2(bar(S_FULL), ph, bar(QFULL0 + st), (i >> 1) & 1, W))) break;  // S(i); L(i) rows
+      // S(i); L(i) rows
+      if (!(ok = warp_wait2(bar(S_FULL0 + (Ly::kSBufs == 2 ? st : 0)), Ly::kSBufs == 2 ? (i >> 1) & 1 : ph,
+                            bar(QFULL0 + st), (i >> 1) & 1, W)))
+        break;
+      const uint32_t tSi = tm + (Ly::kSBufs == 2 && st ? Ly::kColS1 : Ly::kColS);
       ptx::tc_fence_after();
       {
         uint32_t r[32];
-        ptx::tmem_ld32(tm + Ly::kColS + lane_off + c0, r);
+        ptx::tmem_ld32(tSi + lane_off + c0, r);
         const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4 + c0 * 4;
         // key k0 + t is visible to query q0 + col iff col >= t - rel; the
         // block needs the mask unless every entry passes (rel >= 127).
@@ -593,7 +611,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
           for (int k = 0; k < 16; ++k) pk[k] = 0u;
         }
         // P columns [c0, c0 + 16) lie over this warp's own S columns
-        ptx::tmem_st16(tm + Ly::kColS + lane_off + c0, &pk[0]);
+        ptx::tmem_st16(tSi + lane_off + c0, &pk[0]);
         ptx::tmem_st_wait();
       }
       ptx::tc_fence_before();
