@@ -154,12 +154,15 @@ __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict
                                                          int64_t slice_elems, int causal, int kb_rows,
                                                          int64_t offset) {
   constexpr int kPitch = HD + 4;  // floats; keeps 16-byte alignment, staggers banks
+  constexpr int kRows = kTileRows / 2;  // one block per half tile: lane quarters 2 half, 2 half + 1
   extern __shared__ float4 smem_f4[];
   float* tile_s = reinterpret_cast<float*>(smem_f4);
-  const int tile = blockIdx.x % tiles_per_head;
-  const int bh = blockIdx.x / tiles_per_head;
+  const int half = blockIdx.x & 1;
+  const int tile = (blockIdx.x >> 1) % tiles_per_head;
+  const int bh = (blockIdx.x >> 1) / tiles_per_head;
   const int b = bh / H, h = bh % H;
-  const float4* src = reinterpret_cast<const float4*>(acc + dq_unit_offset(bh, tiles_per_head, tile, 0, 0, HD));
+  const float4* src =
+      reinterpret_cast<const float4*>(acc + dq_unit_offset(bh, tiles_per_head, tile, 2 * half, 0, HD));
   // Key blocks that touch this query tile: all, or (causal) those starting at
   // or before the last key its last row sees (row + offset, offset = N_k - N);
   // none when that is negative.  Their slices are summed in increasing order.
@@ -169,9 +172,23 @@ __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict
     last = hi < 0 ? -1 : (hi / kb_rows < last ? (int)(hi / kb_rows) : last);
   }
   const int64_t slice4 = slice_elems / 4;
-  // a tile is 4 x (HD/16) units of [4 column groups][32 rows][4 columns]
+  // a half tile is 2 x (HD/16) units of [4 column groups][32 rows][4 columns];
+  // without slices every load of the thread is issued before the first store
+  constexpr int kLoads = kRows * HD / 4 / 256;
+  if (!kSlices && kLoads * 256 == kRows * HD / 4) {
+    float4 v[kLoads];
+#pragma unroll
+    for (int j = 0; j < kLoads; ++j) v[j] = __ldg(src + threadIdx.x + j * 256);
+#pragma unroll
+    for (int j = 0; j < kLoads; ++j) {
+      const int k = threadIdx.x + j * 256;
+      const int unit = k / 128, g = (k % 128) / 32, r = k % 32;
+      const int row = (unit / (HD / 16)) * 32 + r, col = (unit % (HD / 16)) * 16 + g * 4;
+      *reinterpret_cast<float4*>(tile_s + row * kPitch + col) = v[j];
+    }
+  } else
 #pragma unroll 4
-  for (int k = threadIdx.x; k < kTileRows * HD / 4; k += 256) {
+  for (int k = threadIdx.x; k < kRows * HD / 4; k += 256) {
     const int unit = k / 128, g = (k % 128) / 32, r = k % 32;
     const int row = (unit / (HD / 16)) * 32 + r, col = (unit % (HD / 16)) * 16 + g * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -189,9 +206,9 @@ __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict
   __syncthreads();
   constexpr int kVec = 16 / sizeof(T);           // outputs per 16-byte store
   constexpr int kPerRow = HD / kVec;
-  for (int k = threadIdx.x; k < kTileRows * kPerRow; k += 256) {
+  for (int k = threadIdx.x; k < kRows * kPerRow; k += 256) {
     const int r = k / kPerRow, c = (k % kPerRow) * kVec;
-    const int n = tile * kTileRows + r;
+    const int n = tile * kTileRows + half * kRows + r;
     if (n >= N) continue;
     float v[kVec];
 #pragma unroll
@@ -203,10 +220,10 @@ __global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict
 template <typename T>
 static cudaError_t launch_convert_t(const fa_problem& p, const float* acc, T* dQ, cudaStream_t s) {
   const int tiles = (int)ceil_div(p.N, kTileRows);
-  const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
+  const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles * 2));
 #define FA_CONV_CASE(HDV)                                                                                  \
   case HDV: {                                                                                              \
-    const size_t sm = (size_t)kTileRows * (HDV + 4) * sizeof(float);                                      \
+    const size_t sm = (size_t)(kTileRows / 2) * (HDV + 4) * sizeof(float);                                \
     auto kern = deterministic(p) ? convert_dq_kernel<T, HDV, true> : convert_dq_kernel<T, HDV, false>;    \
     if (sm > 48 * 1024) {                                                                                  \
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);    \
