@@ -95,11 +95,11 @@ static cudaError_t launch_preprocess_t(const fa_problem& p, const T* O, const T*
                                        cudaStream_t s) {
   const int tiles = (int)ceil_div(p.N, kTileRows);
   const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles));
-  // Deterministic, tensor-core kernel: every slice element the convert reads
+  // Deterministic, tensor-core kernels: every slice element the convert reads
   // is written by the backward kernel, so nothing needs zeroing.  The
   // CUDA-core kernel's 64- or 32-row key blocks leave parts of some slices
   // untouched; zero them all.
-  const int zero_slices = !deterministic(p) ? 1 : (tensor_core(p) ? 0 : (int)dq_slices(p));
+  const int zero_slices = !deterministic(p) ? 1 : (tensor_core_bwd(p) ? 0 : (int)dq_slices(p));
   const int64_t slice_elems = dq_slice_elems(p);
 #define FA_PRE_CASE(HDV)                                                                                    \
   case HDV:                                                                                                 \
@@ -370,9 +370,13 @@ fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* 
       !aligned16(dQ_accum) || !aligned16(dK) || !aligned16(dV))
     return FA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (!fa::tensor_core(pn)) return from_cuda(fa::launch_bwd_simt(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, s));
+  if (!fa::tensor_core_bwd(pn))
+    return from_cuda(fa::launch_bwd_simt(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, s));
   int32_t* status = fa::device_status_word();
   if (!status) return FA_ERR_CUDA;
+  if (pn.d == 256)
+    return from_cuda(
+        fa::launch_bwd_d256_sm103(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s));
   return from_cuda(fa::launch_bwd_sm103(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s));
 }
 

@@ -36,13 +36,15 @@ bool normalize_problem(const fa_problem* in, fa_problem* out);  // false: invali
 inline int64_t causal_offset(const fa_problem& p) { return (int64_t)p.N_k - p.N; }
 
 inline bool deterministic(const fa_problem& p) { return (p.flags & FA_FLAG_DETERMINISTIC) != 0; }
-// bf16 with d <= 128 runs on the tensor-core kernels; fp32, and bf16 with
-// d = 256 (whose dK and dV accumulators alone would fill tensor memory), on
-// the CUDA-core kernels.
+// bf16 with d <= 128 runs on the tensor-core kernels; fp32 on the CUDA-core
+// kernels.  bf16 at d = 256 runs the backward on the tensor cores (two CTAs
+// per key block, one per half of the output columns) and the forward on the
+// CUDA-core kernel (fp32 arithmetic).
 inline bool tensor_core(const fa_problem& p) { return p.dtype == FA_BF16 && p.d <= 128; }
-// Key-block height of the backward kernel that serves p (tensor-core kernel:
-// 128; CUDA-core kernel: 64, or 32 at d = 256).
-inline int key_block_rows(const fa_problem& p) { return tensor_core(p) ? 128 : (p.d == 256 ? 32 : 64); }
+inline bool tensor_core_bwd(const fa_problem& p) { return p.dtype == FA_BF16 && (p.d <= 128 || p.d == 256); }
+// Key-block height of the backward kernel that serves p (tensor-core
+// kernels: 128; CUDA-core kernel: 64, or 32 at d = 256).
+inline int key_block_rows(const fa_problem& p) { return tensor_core_bwd(p) ? 128 : (p.d == 256 ? 32 : 64); }
 // dQ accumulator slices: one per key block in deterministic mode, else one.
 inline int64_t dq_slices(const fa_problem& p) {
   return deterministic(p) ? ceil_div(p.N_k, key_block_rows(p)) : 1;
@@ -56,8 +58,8 @@ inline int64_t dq_slice_elems(const fa_problem& p) {
 cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO, float* D,
                               float* dq_accum, cudaStream_t s);
 cudaError_t launch_convert_dq(const fa_problem& p, const float* dq_accum, void* dQ, cudaStream_t s);
-// CUDA-core forward and backward (fp32, and bf16 at d = 256; fp32
-// arithmetic throughout).
+// CUDA-core forward (fp32, and bf16 at d = 256) and backward (fp32); fp32
+// arithmetic throughout.
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
                             void* O, float* L, cudaStream_t s);
 cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
@@ -68,6 +70,11 @@ cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, c
 cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V,
                              const void* dO, const float* L, const float* D, float* dq_accum,
                              void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
+// tcgen05 / TMEM / TMA backward for bf16 at d = 256: two CTAs per key block,
+// each accumulating dK and dV for 128 of the 256 columns.
+cudaError_t launch_bwd_d256_sm103(const fa_problem& p, const void* Q, const void* K, const void* V,
+                                  const void* dO, const float* L, const float* D, float* dq_accum,
+                                  void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
 // The whole backward (preprocess, tcgen05 backward, convert) in one launch
 // of the tcgen05 kernel for bf16, d in {32, 64, 96, 128}; sync holds
 // 1 + 2 B H int32 (zeroed by the launcher).

@@ -1,7 +1,6 @@
 // CUDA-core (FFMA) kernels for float32 problems (tensor cores have no fp32
 // mode that keeps float32 accuracy, and the fp32 workload is a small
-// correctness problem) and for bf16 at d = 256 (whose dK and dV accumulators
-// alone would fill the tensor memory of the tcgen05 kernel); inputs are
+// correctness problem), and the forward for bf16 at d = 256; inputs are
 // widened to fp32 and all arithmetic is fp32:
 //  * the forward pass (online softmax), 64 x 64 tiles;
 //  * the backward pass, 64 x 64 tiles (32 x 32 at d = 256, to fit shared
@@ -418,8 +417,9 @@ cudaError_t launch_bwd_dt(const fa_problem& p, const void* Q, const void* K, con
 
 }  // namespace
 
-// fp32 at every supported d; bf16 only at d = 256 (the tensor-core kernels
-// serve the other bf16 head dims), so only that bf16 instance is built.
+// Forward: fp32 at every supported d; bf16 only at d = 256 (the tensor-core
+// kernels serve the other bf16 head dims), so only that bf16 instance is
+// built.  Backward: fp32 only (every bf16 head dim has a tensor-core kernel).
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                             cudaStream_t s) {
   if (p.dtype == FA_BF16)
@@ -431,9 +431,7 @@ cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, c
 
 cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
                             const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s) {
-  if (p.dtype == FA_BF16)
-    return p.d == 256 ? launch_bwd_t<__nv_bfloat16, 256>(p, Q, K, V, dO, L, D, acc, dK, dV, s)
-                      : cudaErrorInvalidValue;
+  if (p.dtype == FA_BF16) return cudaErrorInvalidValue;
   return launch_bwd_dt<float>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
 }
 

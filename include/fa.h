@@ -45,10 +45,11 @@
  *
  * Supported problems (N is the number of query rows, N_k of key rows; see
  * fa_problem): dtype FA_BF16 with d in {32, 64, 96, 128} (tcgen05
- * tensor-core kernels) or d = 256 (CUDA-core kernels with fp32 arithmetic:
- * at d = 256 the dK and dV accumulators alone would fill tensor memory);
- * dtype FA_FP32 with d in {16, 32, 64, 96, 128, 256} (exact fp32 FFMA
- * kernels, no TF32).  N >= 1, N_k >= 0, B >= 1, H >= 1, N, N_k <= 2^24,
+ * tensor-core kernels) or d = 256 (tensor-core backward with each key block
+ * split over two CTAs by output columns, since the dK and dV accumulators
+ * of one block would fill tensor memory; the forward on a CUDA-core kernel
+ * with fp32 arithmetic); dtype FA_FP32 with d in {16, 32, 64, 96, 128, 256}
+ * (exact fp32 FFMA kernels, no TF32).  N >= 1, N_k >= 0, B >= 1, H >= 1, N, N_k <= 2^24,
  * B*H <= 2^24.
  * Other d return FA_ERR_UNSUPPORTED.
  *
@@ -125,9 +126,9 @@ typedef struct {
 
 /* Number of float32 elements of the dQ accumulator for problem p, or 0 if p
  * is NULL or invalid: B * H * ceil(N/128) * 128 * d, times the number of key
- * blocks with FA_FLAG_DETERMINISTIC: ceil(N_k/128) on the tensor-core kernels
- * (bf16, d <= 128), ceil(N_k/64) on the CUDA-core kernels, ceil(N_k/32) on
- * those at d = 256. */
+ * blocks with FA_FLAG_DETERMINISTIC: ceil(N_k/128) for bf16 (tensor-core
+ * backward), ceil(N_k/64) for fp32 (CUDA-core backward), ceil(N_k/32) for
+ * fp32 at d = 256. */
 size_t fa_dq_accum_elems(const fa_problem* p);
 
 /* Forward pass, companion of the backward: O = softmax(scale Q K^T) V and

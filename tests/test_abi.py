@@ -55,7 +55,8 @@ def test_dq_accum_size(lib):
     assert fa.fa_dq_accum_elems(_prob(d=96, stride_n=96)) == 1 * 2 * 128 * 96
     assert fa.fa_dq_accum_elems(_prob(d=48, stride_n=48)) == 0  # unsupported head dim
     # deterministic: one slice per key block (128 keys on the tensor-core
-    # kernels, 64 on the CUDA-core kernels, 32 on those at d = 256)
+    # kernels, bf16 d = 256 included; 64 on the CUDA-core kernels, 32 on
+    # those at d = 256)
     p = _prob(N=4000, d=128, H=16, B=4, stride_b=16 * 4000 * 128, stride_h=4000 * 128, stride_n=128,
               flags=fa.FA_FLAG_DETERMINISTIC)
     assert fa.fa_dq_accum_elems(p) == 32 * 4 * 16 * 32 * 128 * 128
@@ -63,6 +64,9 @@ def test_dq_accum_size(lib):
               flags=fa.FA_FLAG_DETERMINISTIC)
     assert fa.fa_dq_accum_elems(p) == 1 * 128 * 16
     p = _prob(N=100, d=256, H=1, stride_b=100 * 256, stride_h=100 * 256, stride_n=256,
+              flags=fa.FA_FLAG_DETERMINISTIC)
+    assert fa.fa_dq_accum_elems(p) == 1 * 128 * 256
+    p = _prob(N=100, d=256, H=1, dtype=fa.FA_FP32, stride_b=100 * 256, stride_h=100 * 256, stride_n=256,
               flags=fa.FA_FLAG_DETERMINISTIC)
     assert fa.fa_dq_accum_elems(p) == 4 * 128 * 256
     p = _prob(N=100, d=96, H=1, stride_b=100 * 96, stride_h=100 * 96, stride_n=96, flags=fa.FA_FLAG_DETERMINISTIC)

@@ -1,11 +1,13 @@
 """Head dims beyond 64 and 128: GPU parity against the float64 oracle.
 
 bf16 d = 32 and 96 run on the tensor-core kernels (tiles 64 and 128 columns
-wide, the columns past d zero-filled by the TMA); bf16 d = 256 and fp32
-d = 96, 256 run on the CUDA-core kernels (fp32 arithmetic; 32-row key blocks
-at d = 256).  The oracle is the same plain definition at every d.  Tolerances
-as everywhere: max|dX - ref| / max|ref| <= 2e-2 for bf16 (L <= 1e-3), 1e-5
-for fp32 (L <= 1e-6)."""
+wide, the columns past d zero-filled by the TMA); bf16 d = 256 runs the
+backward on the tensor cores (two CTAs per key block, one per half of the
+columns) and the forward on the CUDA-core kernel; fp32 d = 96, 256 run on the
+CUDA-core kernels (fp32 arithmetic; 32-row key blocks at d = 256).  The
+oracle is the same plain definition at every d.  Tolerances as everywhere:
+max|dX - ref| / max|ref| <= 2e-2 for bf16 (L <= 1e-3), 1e-5 for fp32
+(L <= 1e-6)."""
 
 import pytest
 import torch
