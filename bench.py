@@ -36,8 +36,19 @@ if ROOT not in sys.path:
 
 METRIC = "FA2 backward TFLOPS (10·BHN²d, ½ if causal) and % of GB300 bf16 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_bwd_sm103_traffic.txt")
-KERNEL_SRC = os.path.join(ROOT, "flashattention_backward_gb300", "csrc", "fa_bwd_sm103.cu")
+CSRC = os.path.join(ROOT, "flashattention_backward_gb300", "csrc")
+# per fa_bwd kernel: (kernel name, source file, committed ncu traffic record)
+BWD_KERNELS = {
+    "sm103": ("bwd_sm103_kernel", os.path.join(CSRC, "fa_bwd_sm103.cu"),
+              os.path.join(ROOT, "profiles", "fa_bwd_sm103_traffic.txt")),
+    "d256": ("bwd_d256_kernel", os.path.join(CSRC, "fa_bwd_d256_sm103.cu"),
+             os.path.join(ROOT, "profiles", "fa_bwd_d256_sm103_traffic.txt")),
+}
+
+
+def bwd_kernel(w):
+    """The fa_bwd kernel that serves workload w (bf16)."""
+    return BWD_KERNELS["d256" if w.d == 256 else "sm103"]
 
 
 # ----------------------------------------------------------------- helpers
@@ -51,22 +62,23 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_sha() -> str:
-    with open(KERNEL_SRC, "rb") as f:
+def kernel_sha(src: str) -> str:
+    with open(src, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def recorded_traffic(workload_name: str):
+def recorded_traffic(w):
     """DRAM bytes per fa_bwd launch from the committed ncu summary, or None
     when the kernel source changed since the capture."""
+    _, src, record = bwd_kernel(w)
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(record) as f:
             kv = dict(line.split(None, 1) for line in f.read().splitlines() if line and not line.startswith("#"))
     except (OSError, ValueError):
         return None
-    if kv.get("kernel_sha256", "").strip() != kernel_sha():
+    if kv.get("kernel_sha256", "").strip() != kernel_sha(src):
         return None
-    val = kv.get(f"bytes_per_launch_{workload_name}")
+    val = kv.get(f"bytes_per_launch_{w.name}")
     return float(val) if val else None
 
 
@@ -382,13 +394,13 @@ def main(argv=None) -> int:
         "config": dict(workload_config(w, world), dq_mode="deterministic" if args.deterministic else "atomic"),
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
-        "roofline": {"kernel": "fa_bwd (bwd_sm103_kernel)", "bound": "tensor", "achieved": bwd_tflops,
+        "roofline": {"kernel": f"fa_bwd ({bwd_kernel(w)[0]})", "bound": "tensor", "achieved": bwd_tflops,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": bwd_tflops / peaks["bf16_tflops"],
                      "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback 1.9 PFLOP/s bf16 burst",
                      "frac_of_sustained": bwd_tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
-                     "traffic": recorded_traffic(w.name), "ms": bwd_ms},
+                     "traffic": recorded_traffic(w), "ms": bwd_ms},
         "kernels": {
             "fa_bwd_preprocess": {"ms": pre_ms, "GB/s": pre_bytes / (pre_ms * 1e-3) / 1e9,
                                   "frac_hbm": pre_bytes / (pre_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},

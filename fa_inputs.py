@@ -16,7 +16,11 @@ mha    1 x 32 x 2048 x 64                        none    bf16    N(0,1), torch s
 causal 1 x 32 x 8192 x 128                       causal  bf16    N(0,1), torch seed 2
 ragged 4 x 16 x 4000 x 128                       causal  bf16    N(0,1), torch seed 3
 long   1 x 8 x 32768 x 128                       causal  bf16    Q ~ N(0,16), rest N(0,1), seed 4
+hd256  1 x 16 x 8192 x 256                       causal  bf16    N(0,1), torch seed 5
 =====  =======================================  ======  ======  =====================
+
+``hd256`` is the largest head dim the write-ups' d sweeps reach, at the
+headline sequence length with half the heads (the same bytes per tensor).
 
 The tiny workload mirrors CS349E lecture 11 demo 1: ``numpy.random.default_rng(0)``
 and ``standard_normal((N, d))`` drawn in the order Q, K, V, G (G plays dO).  The
@@ -68,6 +72,7 @@ WORKLOADS = {
     "causal": Workload("causal", 1, 32, 8192, 128, True, "bf16", 2),
     "ragged": Workload("ragged", 4, 16, 4000, 128, True, "bf16", 3),
     "long": Workload("long", 1, 8, 32768, 128, True, "bf16", 4, q_std=4.0),
+    "hd256": Workload("hd256", 1, 16, 8192, 256, True, "bf16", 5),
 }
 
 

@@ -69,10 +69,16 @@ def test_clock_summary_parses_samples_and_reasons():
 
 
 def test_traffic_record_requires_current_kernel_source(tmp_path, monkeypatch):
-    rec = tmp_path / "traffic.txt"
-    rec.write_text(f"# comment\nkernel_sha256 {bench.kernel_sha()}\nbytes_per_launch_causal 1234\n")
-    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(rec))
-    assert bench.recorded_traffic("causal") == 1234.0
-    assert bench.recorded_traffic("mha") is None
-    rec.write_text("kernel_sha256 0000\nbytes_per_launch_causal 1234\n")
-    assert bench.recorded_traffic("causal") is None
+    from fa_inputs import workload
+
+    for key, wname, other in (("sm103", "causal", "mha"), ("d256", "hd256", "causal")):
+        name, src, _ = bench.BWD_KERNELS[key]
+        rec = tmp_path / f"traffic_{key}.txt"
+        rec.write_text(f"# comment\nkernel_sha256 {bench.kernel_sha(src)}\nbytes_per_launch_{wname} 1234\n")
+        monkeypatch.setitem(bench.BWD_KERNELS, key, (name, src, str(rec)))
+        w = workload(wname)
+        assert bench.bwd_kernel(w)[0] == name
+        assert bench.recorded_traffic(w) == 1234.0
+        assert bench.recorded_traffic(w.with_(name=other)) is None
+        rec.write_text(f"kernel_sha256 0000\nbytes_per_launch_{wname} 1234\n")
+        assert bench.recorded_traffic(w) is None
