@@ -17,40 +17,41 @@
 // kernel.  The scores are transposed (TMEM lane = key row), P^T feeds
 // dV += P^T dO from tensor memory, and dS^T goes to shared memory.
 //
-// dQ is produced for a 128-row query tile at a time: dQ = dS K_j[:, half] with
-// the dS of two consecutive 64-row blocks stacked as the 128 rows of the A
-// operand (two 64-query blocks of the MN-major layout), so its rows land in
-// tensor-memory lanes in the accumulator's own tile order.  The walk over
-// query blocks therefore starts on a 128-row tile boundary; a causal block
-// that lies wholly before the diagonal is computed with P = 0.
+// dQ is produced transposed per query block, dQ^T = K_j[:, half]^T dS^T
+// (M = the 128 columns of the half, N = 64 queries), into the tensor-memory
+// columns of the block's dP^T once dS has been formed from it.  The drain
+// warps turn each 4 x 4 piece (4 columns of 4 query rows) around with two
+// rounds of lane shuffles inside groups of four lanes, so that every lane
+// holds 4 consecutive columns of one query row, and add them into the
+// accumulator with vector reductions.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,64) [64,128)    S^T of even / odd query blocks; P^T (bf16) over it
-//   [128,192) [192,256) dP^T of even / odd blocks; the dQ tile of the two
-//                      blocks over both once both dS are in shared memory
+//   [128,192) [192,256) dP^T of even / odd blocks; then dQ^T of that block
 //   [256,384)          dV accumulator (this CTA's 128 columns)
 //   [384,512)          dK accumulator
 //
-// Shared memory: K_j, V_j (4 chunks of 128 rows x 64 columns each), Q_i and
-// dO_i (4 chunks of 64 rows x 64 columns each, one stage), dS^T of two
-// blocks, L and D rows of two blocks, barriers.  The Q and dO chunks of the
-// other CTA's column half are read only by S^T and dP^T, so they are freed
-// (and the next block's loaded) as soon as those products finish; this CTA's
-// own chunks are read again by dK += dS^T Q and dV += P^T dO.  S^T(i+1)
-// contracts over the other half first, while the own half still loads.
+// Shared memory: K_j, V_j (4 chunks of 128 rows x 64 columns each); Q in
+// three regions of two 64 x 64 chunks (a half of the columns of one block
+// each); dO_i (4 chunks of 64 x 64, one stage); dS^T (128 keys x 64
+// queries); L and D rows of two blocks; barriers.  Block i keeps the other
+// CTA's half of Q (read only by S^T) in region i % 3 and its own half (read
+// again by dK += dS^T Q) in region (i + 2) % 3, so both halves of Q(i+1) go
+// into regions freed by S^T(i) and by dK(i-1), and S^T(i+1) can be issued
+// before dS(i) is ready.  dO's halves are freed by dP^T(i) and dV(i), both
+// early in the block.
 //
 // Warp roles (448 threads):
 //   warps 0-7   compute: TMEM lane quarter w % 4, query columns
 //               [32 (w / 4), +32).  P = exp2(S scale log2e - L log2e) -> bf16
 //               into TMEM; dS = P (dP - D) -> bf16 into shared memory.
 //               Epilogue: dV (w < 4), scale * dK (w >= 4).
-//   warps 8-11  dQ drain, one per lane quarter: tensor memory -> registers ->
-//               vector reductions into the accumulator.
+//   warps 8-11  dQ drain, one per lane quarter (32 of the half's columns).
 //   warp 12     TMA producer (K, V once; Q, dO per block; L, D rows).
 //   warp 13     TMEM allocator and MMA issuer (one elected lane issues).
 //
 // MMA issue order per query block i:
-//   dV(i)  S(i+1)[other half]  dK(i)  [dQ(tile) after odd i]  S(i+1)[own half]  dP(i+1)
+//   dV(i)  S(i+1)  dK(i)  dQ^T(i)  dP(i+1)
 //
 // Every wait is bounded; when one runs out the CTA records FA_ERR_TIMEOUT,
 // waits for its own TMA loads and MMAs, frees tensor memory and exits.
@@ -87,14 +88,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 enum BarId {
   KV_FULL = 0,  // K, V landed
-  QO_FULL,      // Q(i): the other half's chunks landed
-  QW_FULL,      // Q(i): this CTA's own chunks landed
-  DOO_FULL,     // dO(i): other half landed
-  DOW_FULL,     // dO(i): own half landed
-  QO_EMPTY,     // S(i) done: Q other-half chunks free
-  QW_EMPTY,     // dK(i) done: Q own chunks free
+  Q_FULL,       // Q(i) landed (both halves)
+  DOO_FULL,     // dO(i): the other half's chunks landed
+  DOW_FULL,     // dO(i): this CTA's own chunks landed
   DOO_EMPTY,    // dP(i) done: dO other-half chunks free
   DOW_EMPTY,    // dV(i) done: dO own chunks free
+  QREG_FREE0,   // Q region r released (by S(i) for i % 3 == r, by dK(i)
+  QREG_FREE1,   //   for (i + 2) % 3 == r)
+  QREG_FREE2,
   LD_FULL0,     // L, D rows of an even / odd block written (32 producer lanes)
   LD_FULL1,
   S_FULL0,      // S^T of an even / odd block in TMEM
@@ -104,9 +105,9 @@ enum BarId {
   P_FULL,       // P^T(i) in TMEM (every compute thread)
   DP_FULL,      // dP^T(i) in TMEM
   DS_FULL,      // dS^T(i) in shared memory (every compute thread)
-  DS_EMPTY,     // dK and dQ of a tile done: both dS^T slots reusable
-  DQ_FULL,      // dQ of a tile in TMEM
-  DQ_EMPTY,     // dQ drained from TMEM (every drain thread)
+  DS_EMPTY,     // dK(i) and dQ^T(i) done: the dS^T buffer is reusable
+  DQ_FULL,      // dQ^T(i) in TMEM
+  DQ_EMPTY,     // dQ^T(i) drained from TMEM (every drain thread)
   ACC_FULL,     // every MMA done: dK, dV final
   kNumBars
 };
@@ -114,18 +115,19 @@ enum BarId {
 struct Ly {
   static constexpr int kKChunk = kKeyRows * 128;  // 128 rows x 128 bytes
   static constexpr int kQChunk = kQRows * 128;    // 64 rows x 128 bytes
+  static constexpr int kQRegion = 2 * kQChunk;    // half of a Q block's columns
   static constexpr int kK = 0;
   static constexpr int kV = kK + 4 * kKChunk;
-  static constexpr int kQ = kV + 4 * kKChunk;
-  static constexpr int kdO = kQ + 4 * kQChunk;
-  static constexpr int kdS = kdO + 4 * kQChunk;         // 2 slots of 128 keys x 64 queries bf16
-  static constexpr int kdSSlot = kKeyRows * 128;
-  static constexpr int kL = kdS + 2 * kdSSlot;          // 2 slots x 64 fp32 (L log2 e)
+  static constexpr int kQ = kV + 4 * kKChunk;           // 3 regions
+  static constexpr int kdO = kQ + 3 * kQRegion;
+  static constexpr int kdS = kdO + 4 * kQChunk;         // 128 keys x 64 queries bf16
+  static constexpr int kdSBytes = kKeyRows * 128;
+  static constexpr int kL = kdS + kdSBytes;             // 2 slots x 64 fp32 (L log2 e)
   static constexpr int kD = kL + 2 * kQRows * 4;        // 2 slots x 64 fp32
   static constexpr int kBar = kD + 2 * kQRows * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
   static constexpr int kBytes = kMisc + 16;
-  static constexpr uint32_t kColS0 = 0, kColS1 = 64, kColdP0 = 128, kColdP1 = 192, kColdQ = 128;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 64, kColdP0 = 128, kColdP1 = 192;
   static constexpr uint32_t kColdV = 256, kColdK = 384;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -178,22 +180,34 @@ __device__ __forceinline__ void store_row128(uint32_t taddr, bool valid, __nv_bf
   }
 }
 
-// 32 fp32 columns (two 16-column units) of one query row into the dQ
-// accumulator: unit u, column group g at float offset u * 512 + g * 128 + row * 4.
-template <bool kDet>
-__device__ __forceinline__ void drain32(float* unit0, int lane, const uint32_t (&r)[32]) {
-#pragma unroll
-  for (int v = 0; v < 2; ++v)
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float* p = unit0 + v * kDqUnitFloats + g * 128 + lane * 4;
-      const float a = __uint_as_float(r[16 * v + 4 * g]), b = __uint_as_float(r[16 * v + 4 * g + 1]);
-      const float c = __uint_as_float(r[16 * v + 4 * g + 2]), d = __uint_as_float(r[16 * v + 4 * g + 3]);
-      if (kDet)
-        ptx::st_global_v4(p, a, b, c, d);
-      else
-        ptx::red_add_v4(p, a, b, c, d);
-    }
+// Transpose of a 4 x 4 piece held by four lanes (lane b of the group holds
+// x[k] = piece[k][b]): afterwards lane b holds x[j] = piece[b][j].  Two
+// rounds of exchanges with the partner lane b ^ 2, then b ^ 1, each moving
+// the two entries that belong to the partner's half.
+__device__ __forceinline__ void quad_transpose(float (&x)[4], int b) {
+  const bool hi2 = (b & 2) != 0;
+  float a0 = hi2 ? x[0] : x[2], a1 = hi2 ? x[1] : x[3];
+  a0 = __shfl_xor_sync(0xffffffffu, a0, 2);
+  a1 = __shfl_xor_sync(0xffffffffu, a1, 2);
+  if (hi2) {
+    x[0] = a0;
+    x[1] = a1;
+  } else {
+    x[2] = a0;
+    x[3] = a1;
+  }
+  const bool hi1 = (b & 1) != 0;
+  a0 = hi1 ? x[0] : x[1];
+  a1 = hi1 ? x[2] : x[3];
+  a0 = __shfl_xor_sync(0xffffffffu, a0, 1);
+  a1 = __shfl_xor_sync(0xffffffffu, a1, 1);
+  if (hi1) {
+    x[0] = a0;
+    x[2] = a1;
+  } else {
+    x[1] = a0;
+    x[3] = a1;
+  }
 }
 
 template <bool kDet>
@@ -228,14 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(KV_FULL), 1);
-    ptx::mbar_init(bar(QO_FULL), 1);
-    ptx::mbar_init(bar(QW_FULL), 1);
+    ptx::mbar_init(bar(Q_FULL), 1);
     ptx::mbar_init(bar(DOO_FULL), 1);
     ptx::mbar_init(bar(DOW_FULL), 1);
-    ptx::mbar_init(bar(QO_EMPTY), 1);
-    ptx::mbar_init(bar(QW_EMPTY), 1);
     ptx::mbar_init(bar(DOO_EMPTY), 1);
     ptx::mbar_init(bar(DOW_EMPTY), 1);
+    ptx::mbar_init(bar(QREG_FREE0), 1);
+    ptx::mbar_init(bar(QREG_FREE1), 1);
+    ptx::mbar_init(bar(QREG_FREE2), 1);
     ptx::mbar_init(bar(LD_FULL0), 32);
     ptx::mbar_init(bar(LD_FULL1), 32);
     ptx::mbar_init(bar(S_FULL0), 1);
@@ -262,21 +276,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tm = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
   const int k0 = kb * kKeyRows;
-  // first 128-row query tile holding a query that sees key k0 (i >= k0 - offset)
-  const int tile_first = !prm.causal ? 0 : (k0 > prm.offset ? (k0 - prm.offset) / kKeyRows : 0);
-  const int blk_first = 2 * tile_first;               // in 64-row query blocks
-  const int n_iter = 2 * (prm.n_tiles - tile_first);  // even: whole tiles
+  // first 64-row query block holding a query that sees key k0
+  // (i >= k0 - offset; every key block has one, the last query sees every key)
+  const int blk_first = !prm.causal ? 0 : (k0 > prm.offset ? (k0 - prm.offset) / kQRows : 0);
+  const int n_iter = (prm.N + kQRows - 1) / kQRows - blk_first;
   const int64_t khead = (int64_t)b * prm.ksb + (int64_t)hh * prm.ksh;
   const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
   const int own = 2 * hf, other = 2 * (1 - hf);  // first 64-column chunk of each half
 
   const uint32_t sK = sbase + Ly::kK, sV = sbase + Ly::kV, sQ = sbase + Ly::kQ, sdO = sbase + Ly::kdO;
   const uint32_t sdS = sbase + Ly::kdS;
+  // Q regions of block i: the other half in i % 3, this CTA's half in (i + 2) % 3
+  auto q_other = [&](int i) -> int { return i % 3; };
+  auto q_own = [&](int i) -> int { return (i + 2) % 3; };
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     bool ok = true;
-    int n_qo = 0, n_qw = 0, n_doo = 0, n_dow = 0;  // loads issued per barrier
+    int n_q = 0, n_doo = 0, n_dow = 0;  // loads issued per barrier
+    int reg_loads0 = 0, reg_loads1 = 0, reg_loads2 = 0;  // loads into each Q region so far
     if (lane == 0) {
       ptx::prefetch_tensormap(&tmQ);
       ptx::prefetch_tensormap(&tmK);
@@ -301,18 +319,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         dv[u] = q < prm.N ? __ldg(prm.D + (int64_t)bh * prm.N + q) : 0.f;
       }
     };
-    auto load_half = [&](const CUtensorMap* map, uint32_t tile, int c, uint32_t full, int q0) {
-      ptx::mbar_arrive_expect_tx(full, 2 * Ly::kQChunk);
-      ptx::tma_load_4d(tile + c * Ly::kQChunk, map, full, c * 64, q0, hh, b);
-      ptx::tma_load_4d(tile + (c + 1) * Ly::kQChunk, map, full, (c + 1) * 64, q0, hh, b);
+    // two 64 x 64 chunks (columns c, c + 1) of a 64-row block
+    auto load2 = [&](const CUtensorMap* map, uint32_t dst, int c, uint32_t full, int q0) {
+      ptx::tma_load_4d(dst, map, full, c * 64, q0, hh, b);
+      ptx::tma_load_4d(dst + Ly::kQChunk, map, full, (c + 1) * 64, q0, hh, b);
+    };
+    // a Q region may be refilled once its previous contents' reader is done
+    auto region_free = [&](int r) -> bool {
+      int n;
+      if (r == 0)
+        n = reg_loads0++;
+      else if (r == 1)
+        n = reg_loads1++;
+      else
+        n = reg_loads2++;
+      return n == 0 || warp_wait(bar(QREG_FREE0 + r), (n - 1) & 1, W);
     };
     fetch_rows(0);
     for (int i = 0; i < n_iter; ++i) {
       const int q0 = (blk_first + i) * kQRows;
       const uint32_t pp = (i - 1) & 1;  // phase of the previous block's release
-      // L, D rows into slot i & 1 (its last reader, dS(i-2), finished before
-      // S(i-1) was issued, i.e. before QO_EMPTY(i-1))
-      if (i >= 1 && !(ok = warp_wait(bar(QO_EMPTY), pp, W))) break;
+      // Q(i): both regions free (their last readers were dK(i-2) and S(i-1),
+      // which also means dS(i-2) is done with L, D slot i & 1)
+      if (!(ok = region_free(q_other(i)) && region_free(q_own(i)))) break;
       float* sL = reinterpret_cast<float*>(smem + Ly::kL) + (i & 1) * kQRows;
       float* sD = reinterpret_cast<float*>(smem + Ly::kD) + (i & 1) * kQRows;
       sL[lane] = lv[0];
@@ -320,25 +349,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       sD[lane] = dv[0];
       sD[lane + 32] = dv[1];
       ptx::mbar_arrive(bar(LD_FULL0 + (i & 1)));
-      if (lane == 0) load_half(&tmQ, sQ, other, bar(QO_FULL), q0);
-      n_qo = i + 1;
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(Q_FULL), 4 * Ly::kQChunk);
+        load2(&tmQ, sQ + q_other(i) * Ly::kQRegion, other, bar(Q_FULL), q0);
+        load2(&tmQ, sQ + q_own(i) * Ly::kQRegion, own, bar(Q_FULL), q0);
+      }
+      n_q = i + 1;
       if (i >= 1 && !(ok = warp_wait(bar(DOO_EMPTY), pp, W))) break;
-      if (lane == 0) load_half(&tmdO, sdO, other, bar(DOO_FULL), q0);
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(DOO_FULL), 2 * Ly::kQChunk);
+        load2(&tmdO, sdO + other * Ly::kQChunk, other, bar(DOO_FULL), q0);
+      }
       n_doo = i + 1;
       if (i >= 1 && !(ok = warp_wait(bar(DOW_EMPTY), pp, W))) break;
-      if (lane == 0) load_half(&tmdO, sdO, own, bar(DOW_FULL), q0);
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(DOW_FULL), 2 * Ly::kQChunk);
+        load2(&tmdO, sdO + own * Ly::kQChunk, own, bar(DOW_FULL), q0);
+      }
       n_dow = i + 1;
-      if (i >= 1 && !(ok = warp_wait(bar(QW_EMPTY), pp, W))) break;
-      if (lane == 0) load_half(&tmQ, sQ, own, bar(QW_FULL), q0);
-      n_qw = i + 1;
       __syncwarp();
       if (i + 1 < n_iter) fetch_rows(i + 1);
     }
     if (!ok) {  // let every copy this CTA started land before the CTA exits
       ptx::wait_bounded(bar(KV_FULL), 0, W, false);
-      // one stage: only the last load on each barrier can still be in flight
-      if (n_qo) ptx::wait_bounded(bar(QO_FULL), (n_qo - 1) & 1, W, false);
-      if (n_qw) ptx::wait_bounded(bar(QW_FULL), (n_qw - 1) & 1, W, false);
+      // each barrier's earlier loads were consumed before the next was issued
+      if (n_q) ptx::wait_bounded(bar(Q_FULL), (n_q - 1) & 1, W, false);
       if (n_doo) ptx::wait_bounded(bar(DOO_FULL), (n_doo - 1) & 1, W, false);
       if (n_dow) ptx::wait_bounded(bar(DOW_FULL), (n_dow - 1) & 1, W, false);
     }
@@ -346,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issue
     constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, kQRows, false, false);  // S^T, dP^T
     constexpr uint32_t kIdKV = ptx::idesc_bf16_f32(128, kHalfD, false, true);  // dV, dK
-    constexpr uint32_t kIdQ = ptx::idesc_bf16_f32(128, kHalfD, true, true);    // dQ
+    constexpr uint32_t kIdQ = ptx::idesc_bf16_f32(128, kQRows, true, true);    // dQ^T
     // K-major operand, 16-element K step kk inside 64-column chunks
     auto kdesc = [&](uint32_t tile, uint32_t chunk, int kk) -> uint64_t {
       return ptx::sdesc_sw128(tile + (kk >> 2) * chunk + (kk & 3) * 32, 16, 1024);
@@ -357,43 +392,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto tS = [&](int i) -> uint32_t { return tm + ((i & 1) ? Ly::kColS1 : Ly::kColS0); };
     auto tdP = [&](int i) -> uint32_t { return tm + ((i & 1) ? Ly::kColdP1 : Ly::kColdP0); };
-    const uint32_t tdQ = tm + Ly::kColdQ, tdV = tm + Ly::kColdV, tdK = tm + Ly::kColdK;
-    // 16-column K steps of one 128-column half of S^T = K Q^T or dP^T = V dO^T
-    auto issue_half = [&](uint32_t d, uint32_t a_tile, uint32_t b_tile, int c, bool first) {
+    const uint32_t tdV = tm + Ly::kColdV, tdK = tm + Ly::kColdK;
+    // S^T(i) = K Q(i)^T, 16 K steps over the 256 columns; the Q chunk of
+    // column block c sits in the region of its half
+    auto issue_S = [&](int i) {
+      const uint32_t qo = sQ + q_other(i) * Ly::kQRegion, qw = sQ + q_own(i) * Ly::kQRegion;
+#pragma unroll
+      for (int kk = 0; kk < kHD / 16; ++kk) {
+        const int c = kk >> 2;
+        const uint32_t qb = (c >> 1) == hf ? qw : qo;
+        ptx::mma_ss(tS(i), kdesc(sK, Ly::kKChunk, kk), kdesc(qb + (c & 1) * Ly::kQChunk, 0, kk & 3), kIdS, kk > 0);
+      }
+      ptx::tc_commit(bar(S_FULL0 + (i & 1)));
+      ptx::tc_commit(bar(QREG_FREE0 + q_other(i)));
+    };
+    // dP^T(i) = V dO(i)^T, in two halves (each as soon as its chunks landed)
+    auto issue_dP_half = [&](int i, int c, bool first) {
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int kk = 4 * c + s;
-        ptx::mma_ss(d, kdesc(a_tile, Ly::kKChunk, kk), kdesc(b_tile, Ly::kQChunk, kk), kIdS, !(first && s == 0));
+        ptx::mma_ss(tdP(i), kdesc(sV, Ly::kKChunk, kk), kdesc(sdO, Ly::kQChunk, kk), kIdS, !(first && s == 0));
       }
     };
 
-    bool ok = warp_wait(bar(KV_FULL), 0, W) && warp_wait(bar(QO_FULL), 0, W);
+    bool ok = warp_wait(bar(KV_FULL), 0, W) && warp_wait(bar(Q_FULL), 0, W);
     if (ok) {
       ptx::tc_fence_after();
-      if (ptx::elect_one()) issue_half(tS(0), sK, sQ, other, true);
-      __syncwarp();
-      ok = warp_wait(bar(QW_FULL), 0, W);
-    }
-    if (ok) {
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) {
-        issue_half(tS(0), sK, sQ, own, false);
-        ptx::tc_commit(bar(S_FULL0));
-        ptx::tc_commit(bar(QO_EMPTY));
-      }
+      if (ptx::elect_one()) issue_S(0);
       __syncwarp();
       ok = warp_wait(bar(DOO_FULL), 0, W);
     }
     if (ok) {
       ptx::tc_fence_after();
-      if (ptx::elect_one()) issue_half(tdP(0), sV, sdO, other, true);
+      if (ptx::elect_one()) issue_dP_half(0, other, true);
       __syncwarp();
       ok = warp_wait(bar(DOW_FULL), 0, W);
     }
     if (ok) {
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
-        issue_half(tdP(0), sV, sdO, own, false);
+        issue_dP_half(0, own, false);
         ptx::tc_commit(bar(DP_FULL));
         ptx::tc_commit(bar(DOO_EMPTY));
       }
@@ -416,59 +454,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit(bar(DOW_EMPTY));
       }
       __syncwarp();
-      // S^T(i+1), other half, once its Q chunks have landed and the S buffer's
-      // last reader dV(i-1) is done
+      // S^T(i+1) once Q(i+1) has landed and the S buffer's last reader dV(i-1)
+      // is done, so that it is ready when the compute warps finish dS(i)
       if (more) {
-        ok = i >= 1 ? warp_wait2(bar(QO_FULL), ph1, bar(DV_DONE0 + ((i + 1) & 1)), ((i - 1) >> 1) & 1, W)
-                    : warp_wait(bar(QO_FULL), ph1, W);
+        ok = i >= 1 ? warp_wait2(bar(Q_FULL), ph1, bar(DV_DONE0 + ((i + 1) & 1)), ((i - 1) >> 1) & 1, W)
+                    : warp_wait(bar(Q_FULL), ph1, W);
         if (!ok) break;
         ptx::tc_fence_after();
-        if (ptx::elect_one()) issue_half(tS(i + 1), sK, sQ, other, true);
+        if (ptx::elect_one()) issue_S(i + 1);
         __syncwarp();
       }
-      // dK += dS^T Q[:, own]; after an odd block, dQ of the tile:
-      // dQ = [dS(i-1); dS(i)] K[:, own] (A: the two dS^T slots as the two
-      // 64-query MN blocks)
+      // dK += dS^T Q[:, own]; then dQ^T = K[:, own]^T dS^T into the columns
+      // of dP^T(i) (read by the compute warps before DS_FULL), once the drain
+      // has emptied the other dP^T buffer for dP(i+1)
       if (!(ok = warp_wait(bar(DS_FULL), ph, W))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
-        const uint32_t slot = sdS + (i & 1) * Ly::kdSSlot;
+        const uint32_t qw = sQ + q_own(i) * Ly::kQRegion;
 #pragma unroll
         for (int kk = 0; kk < kQRows / 16; ++kk)
-          ptx::mma_ss(tdK, kdesc(slot, Ly::kdSSlot, kk), mndesc(sQ + own * Ly::kQChunk, Ly::kQChunk, kk), kIdKV,
-                      (i | kk) != 0);
-        ptx::tc_commit(bar(QW_EMPTY));
-        if (i & 1) {
+          ptx::mma_ss(tdK, kdesc(sdS, 0, kk), mndesc(qw, Ly::kQChunk, kk), kIdKV, (i | kk) != 0);
+        ptx::tc_commit(bar(QREG_FREE0 + q_own(i)));
+      }
+      __syncwarp();
+      if (i >= 1 && !(ok = warp_wait(bar(DQ_EMPTY), (i - 1) & 1, W))) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kKeyRows / 16; ++kk)
-            ptx::mma_ss(tdQ, mndesc(sdS, Ly::kdSSlot, kk), mndesc(sK + own * Ly::kKChunk, Ly::kKChunk, kk), kIdQ,
-                        kk > 0);
-          ptx::tc_commit(bar(DQ_FULL));
-          ptx::tc_commit(bar(DS_EMPTY));
-        }
+        for (int kk = 0; kk < kKeyRows / 16; ++kk)
+          ptx::mma_ss(tdP(i), mndesc(sK + own * Ly::kKChunk, Ly::kKChunk, kk), mndesc(sdS, Ly::kdSBytes, kk), kIdQ,
+                      kk > 0);
+        ptx::tc_commit(bar(DQ_FULL));
+        ptx::tc_commit(bar(DS_EMPTY));
       }
       __syncwarp();
       if (!more) break;
-      // S^T(i+1), own half
-      if (!(ok = warp_wait(bar(QW_FULL), ph1, W))) break;
+      // dP^T(i+1), each half of the columns as soon as its dO chunks landed
+      if (!(ok = warp_wait(bar(DOO_FULL), ph1, W))) break;
       ptx::tc_fence_after();
-      if (ptx::elect_one()) {
-        issue_half(tS(i + 1), sK, sQ, own, false);
-        ptx::tc_commit(bar(S_FULL0 + ((i + 1) & 1)));
-        ptx::tc_commit(bar(QO_EMPTY));
-      }
-      __syncwarp();
-      // dP^T(i+1); an even block's columns held the dQ tile just drained
-      ok = (i & 1) ? warp_wait2(bar(DQ_EMPTY), (i >> 1) & 1, bar(DOO_FULL), ph1, W)
-                   : warp_wait(bar(DOO_FULL), ph1, W);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) issue_half(tdP(i + 1), sV, sdO, other, true);
+      if (ptx::elect_one()) issue_dP_half(i + 1, other, true);
       __syncwarp();
       if (!(ok = warp_wait(bar(DOW_FULL), ph1, W))) break;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
-        issue_half(tdP(i + 1), sV, sdO, own, false);
+        issue_dP_half(i + 1, own, false);
         ptx::tc_commit(bar(DP_FULL));
         ptx::tc_commit(bar(DOO_EMPTY));
       }
@@ -479,25 +508,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
   } else if (warp >= kDrainWarp0) {
     // ------------------------------------------------------------ dQ drain
-    // One warp per TMEM lane quarter (32 query rows of the tile): this CTA's
-    // 128 columns are eight 16-column units, contiguous in the accumulator.
+    // Warp qq holds TMEM lanes 32 qq .. +31, i.e. columns hf*128 + 32 qq + lane
+    // of dQ, for the 64 query rows of the block (TMEM columns).  Lane 4a + b
+    // transposes with its group so that it holds columns 4a .. 4a + 3 of
+    // query rows 4m + b, one 16-byte piece of the accumulator layout each.
     const int qq = warp & 3;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-    const uint32_t src = tm + Ly::kColdQ + lane_off;
-    for (int t = 0; t < n_iter / 2; ++t) {
-      if (!warp_wait(bar(DQ_FULL), t & 1, W)) break;
+    const int ga = lane >> 2, gb = lane & 3;
+    const int cb = hf * (kHalfD / 16) + 2 * qq + (ga >> 2);  // 16-column block
+    const int cg = ga & 3;                                    // 4-column group in it
+    for (int i = 0; i < n_iter; ++i) {
+      if (!warp_wait(bar(DQ_FULL), i & 1, W)) break;
       ptx::tc_fence_after();
-      float* dst = prm.dq_accum + (kDet ? kb * prm.slice_elems : 0) +
-                   dq_unit_offset(bh, prm.n_tiles, tile_first + t, qq, hf * (kHalfD / 16), kHD);
       uint32_t r[64];
-      ptx::tmem_ld64(src, src + 32, r);
-      drain32<kDet>(dst, lane, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
-      drain32<kDet>(dst + 2 * kDqUnitFloats, lane, *reinterpret_cast<const uint32_t(*)[32]>(&r[32]));
-      ptx::tmem_ld64(src + 64, src + 96, r);
+      ptx::tmem_ld64(tm + ((i & 1) ? Ly::kColdP1 : Ly::kColdP0) + lane_off,
+                     tm + ((i & 1) ? Ly::kColdP1 : Ly::kColdP0) + lane_off + 32, r);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(DQ_EMPTY));  // the columns are free for dP
-      drain32<kDet>(dst + 4 * kDqUnitFloats, lane, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
-      drain32<kDet>(dst + 6 * kDqUnitFloats, lane, *reinterpret_cast<const uint32_t(*)[32]>(&r[32]));
+      ptx::mbar_arrive(bar(DQ_EMPTY));  // the columns are free for dP(i+2)
+      const int blk = blk_first + i;    // 64-row block: tile blk / 2, rows 64 (blk % 2) + ...
+      float* base = prm.dq_accum + (kDet ? kb * prm.slice_elems : 0) +
+                    dq_unit_offset(bh, prm.n_tiles, blk >> 1, 0, cb, kHD) + cg * 128;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        float x[4] = {__uint_as_float(r[4 * m]), __uint_as_float(r[4 * m + 1]), __uint_as_float(r[4 * m + 2]),
+                      __uint_as_float(r[4 * m + 3])};
+        quad_transpose(x, gb);
+        const int row = (blk & 1) * kQRows + 4 * m + gb;  // query row inside the 128-row tile
+        float* p = base + (int64_t)(row >> 5) * (kHD / 16) * kDqUnitFloats + (row & 31) * 4;
+        if (kDet)
+          ptx::st_global_v4(p, x[0], x[1], x[2], x[3]);
+        else
+          ptx::red_add_v4(p, x[0], x[1], x[2], x[3]);
+      }
     }
   } else {
     // ------------------------------------------------------------ compute
@@ -557,10 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(P_FULL));
-      // ---- dS(i) into slot i & 1, once dK and dQ of the previous tile have
-      // read both slots (checked at the first block of each tile)
-      ok = ((i & 1) == 0 && i >= 2) ? warp_wait2(bar(DP_FULL), ph, bar(DS_EMPTY), ((i >> 1) - 1) & 1, W)
-                                    : warp_wait(bar(DP_FULL), ph, W);
+      // ---- dS(i), once dK(i-1) and dQ^T(i-1) have read the buffer
+      ok = i >= 1 ? warp_wait2(bar(DP_FULL), ph, bar(DS_EMPTY), ph ^ 1, W) : warp_wait(bar(DP_FULL), ph, W);
       if (!ok) break;
       ptx::tc_fence_after();
       {
@@ -580,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // row t of dS^T (64 queries = 128 bytes), 16-byte pieces 4G .. 4G+3,
         // 128-byte swizzle (piece XOR row % 8)
-        const uint32_t row = sdS + (i & 1) * Ly::kdSSlot + t * 128;
+        const uint32_t row = sdS + t * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint32_t piece = (uint32_t)(G * 4 + u);
