@@ -99,7 +99,7 @@ static cudaError_t launch_preprocess_t(const fa_problem& p, const T* O, const T*
   // is written by the backward kernel, so nothing needs zeroing.  The
   // CUDA-core kernel's 64- or 32-row key blocks leave parts of some slices
   // untouched; zero them all.
-  const int zero_slices = !deterministic(p) ? 1 : (tensor_core_bwd(p) ? 0 : (int)dq_slices(p));
+  const int zero_slices = !deterministic(p) ? 1 : (tensor_core(p) ? 0 : (int)dq_slices(p));
   const int64_t slice_elems = dq_slice_elems(p);
 #define FA_PRE_CASE(HDV)                                                                                    \
   case HDV:                                                                                                 \
@@ -370,7 +370,7 @@ fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* 
       !aligned16(dQ_accum) || !aligned16(dK) || !aligned16(dV))
     return FA_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  if (!fa::tensor_core_bwd(pn))
+  if (!fa::tensor_core(pn))
     return from_cuda(fa::launch_bwd_simt(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, s));
   int32_t* status = fa::device_status_word();
   if (!status) return FA_ERR_CUDA;
@@ -404,7 +404,7 @@ fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const v
 
 size_t fa_backward_fused_sync_elems(const fa_problem* p) {
   fa_problem pn;
-  if (normalize(p, &pn) != FA_OK || !fa::tensor_core(pn)) return 0;
+  if (normalize(p, &pn) != FA_OK || !fa::fused_supported(pn)) return 0;
   return 1 + 2 * (size_t)pn.B * pn.H;
 }
 
@@ -414,7 +414,7 @@ fa_status fa_backward_fused(const fa_problem* p, const void* Q, const void* K, c
   fa_problem pn;
   fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
-  if (!fa::tensor_core(pn)) return FA_ERR_UNSUPPORTED;
+  if (!fa::fused_supported(pn)) return FA_ERR_UNSUPPORTED;
   if (fa::fused_items(pn) > 0x7fffffff) return FA_ERR_UNSUPPORTED;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(dO) || !aligned16(L) ||
       !aligned16(D) || !aligned16(dQ_accum) || !aligned16(dQ) || !aligned16(dK) || !aligned16(dV) || !sync ||

@@ -664,10 +664,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [B, H, rows, 256] bf16 (Q-shaped: kv = false, K-shaped: kv = true) as a
-// 4-D TMA map with boxes of 64 columns x box_rows rows, 128-byte swizzle;
-// rows past the end read as zeros.
-bool make_map(CUtensorMap* m, const void* base, const fa_problem& p, bool kv, int box_rows) {
+}  // namespace
+
+// [B, H, rows, d] bf16 (Q-shaped: kv = false, K-shaped: kv = true) as a 4-D
+// TMA map with boxes of 64 columns x box_rows rows, 128-byte swizzle; rows
+// past the end and columns past d read as zeros.
+bool make_bf16_tile_map_rows(CUtensorMap* m, const void* base, const fa_problem& p, bool kv, int box_rows) {
   auto enc = encode_fn();
   if (!enc) return false;
   const int64_t rows = kv ? p.N_k : p.N;
@@ -682,6 +684,8 @@ bool make_map(CUtensorMap* m, const void* base, const fa_problem& p, bool kv, in
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <bool kDet>
 cudaError_t launch_t(const CUtensorMap* maps, const D256Params& prm, cudaStream_t s) {
@@ -700,8 +704,8 @@ cudaError_t launch_bwd_d256_sm103(const fa_problem& p, const void* Q, const void
                                   int32_t* status, uint64_t wait_ns, cudaStream_t s) {
   if (p.d != kHD || p.dtype != FA_BF16) return cudaErrorInvalidValue;
   CUtensorMap maps[4];
-  if (!make_map(&maps[0], Q, p, false, kQRows) || !make_map(&maps[1], K, p, true, kKeyRows) ||
-      !make_map(&maps[2], V, p, true, kKeyRows) || !make_map(&maps[3], dO, p, false, kQRows))
+  if (!make_bf16_tile_map_rows(&maps[0], Q, p, false, kQRows) || !make_bf16_tile_map_rows(&maps[1], K, p, true, kKeyRows) ||
+      !make_bf16_tile_map_rows(&maps[2], V, p, true, kKeyRows) || !make_bf16_tile_map_rows(&maps[3], dO, p, false, kQRows))
     return cudaErrorInvalidValue;
   D256Params prm;
   prm.L = L;

@@ -1,5 +1,6 @@
-// Forward pass (companion of the backward) for bf16, head dim 32, 64, 96 or 128, on
-// the sm_100-family tensor cores.  Online softmax over 128-key blocks
+// Forward pass (companion of the backward) for bf16, head dim 32, 64, 96, 128 or
+// 256, on the sm_100-family tensor cores.  Online softmax over key blocks of
+// 128 keys (64 at d = 256)
 // (1point3acres FlashAttention write-up, online-softmax paragraphs; "CUDA
 // 算子工程" ch.16 §16.4 for L = m + log l):
 //   m' = max(m, rowmax(S_b)),  alpha = exp(m - m'),  l' = alpha l + sum(p_b),
@@ -12,8 +13,11 @@
 // in TMEM.  With three buffers S_{b+2} is issued as soon as O += P_{b-1} V_{b-1}
 // has read its buffer, ahead of O += P_b V_b, so the tensor pipe computes the
 // score block two ahead while the softmax warps still work on P_b.
-// K lives in three shared-memory stages, each freed as soon as its S block
-// is done; V in two, each freed when its O += P V is done.
+// K lives in three shared-memory stages (two at d = 256), each freed as soon
+// as its S block is done; V in two, each freed when its O += P V is done.
+// At d = 256 the 64-key blocks keep a 64 KB Q tile and two stages each of K
+// and V (32 KB a tile) inside shared memory, and O takes tensor-memory
+// columns 256-511 beside three 64-column S buffers.
 //
 // The exponent base m is only moved when a row maximum grows by more than
 // 2^8 (in exp2 units): otherwise P = exp2(S - m) <= 256 stays well inside
@@ -23,7 +27,7 @@
 //
 // Warp roles (352 threads):
 //   warps 0-7  softmax.  Warp w owns query rows 32*(w%4) .. +31 (its TMEM lane
-//              quarter) and key columns [64*(w/4), +64) of each block; the two
+//              quarter) and the key columns of half w/4 of each block; the two
 //              warps of a lane quarter exchange row maxima through shared
 //              memory.  Epilogue: O columns [d/2 * (w/4), +d/2) and L.
 //   warp  8    TMA producer of Q (once) and K.
@@ -45,13 +49,15 @@
 namespace fa {
 
 bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p, bool kv);  // fa_bwd_sm103.cu
+bool make_bf16_tile_map_rows(CUtensorMap* m, const void* base, const fa_problem& p, bool kv,
+                             int box_rows);  // fa_bwd_d256_sm103.cu
 
 namespace {
 
 constexpr int kBlk = 128;
 constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kKStages = 3;  // K tiles in shared memory
+constexpr int kKStages = 3;  // K tiles in shared memory (at most; two at d = 256)
 constexpr int kVStages = 2;  // V tiles in shared memory
 constexpr int kSBufs = 3;    // S/P buffers in TMEM
 constexpr int kHeadGroup = 4;  // heads whose query blocks interleave in the grid order
@@ -77,22 +83,27 @@ enum BarId {
   kNumBars
 };
 
-// Tiles LD = 64 or 128 columns wide: head dims 32 and 64 use LD = 64, 96 and
-// 128 use LD = 128; the TMA zero-fills the columns past d.
+// Tiles LD = 64, 128 or 256 columns wide: head dims 32 and 64 use LD = 64, 96
+// and 128 use LD = 128, 256 uses LD = 256; the TMA zero-fills the columns
+// past d.  Key blocks are BK rows: 128, or 64 at LD = 256.
 template <int LD>
 struct FwdLayout {
-  static constexpr int kChunk = kBlk * 128;
-  static constexpr int kTile = kBlk * LD * 2;
+  static constexpr int BK = LD == 256 ? 64 : 128;       // keys per block
+  static constexpr int kKSt = LD == 256 ? 2 : kKStages;  // K stages
+  static constexpr int kQChunk = kBlk * 128;            // 128 rows x 64 columns
+  static constexpr int kKVChunk = BK * 128;             // BK rows x 64 columns
+  static constexpr int kQTile = kBlk * LD * 2;
+  static constexpr int kKVTile = BK * LD * 2;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;                 // kKStages tiles
-  static constexpr int kV = kK + kKStages * kTile;      // kVStages tiles
-  static constexpr int kX = kV + kVStages * kTile;      // exchange: [2 parities (max) + 1 (sum)][2 halves][128] fp32
+  static constexpr int kK = kQ + kQTile;                // kKSt tiles
+  static constexpr int kV = kK + kKSt * kKVTile;        // kVStages tiles
+  static constexpr int kX = kV + kVStages * kKVTile;    // exchange: [2 parities (max) + 1 (sum)][2 halves][128] fp32
   static constexpr int kBar = kX + 3 * 2 * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
-  static constexpr uint32_t kColO = kSBufs * 128;     // S/P buffers at 0, 128, 256
+  static constexpr uint32_t kColO = LD == 256 ? 256 : kSBufs * BK;  // S/P buffers at 0, BK, 2 BK
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kColO + LD <= kTmemCols, "tensor memory budget");
+  static_assert(kSBufs * BK <= kColO && kColO + LD <= kTmemCols, "tensor memory budget");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -106,7 +117,7 @@ struct FwdParams {
   int64_t sb, sh, sn;
   float scale;
   int causal;
-  int Nk, nk_tiles;  // key rows, key blocks
+  int Nk;            // key rows
   int offset;        // Nk - N: key j visible to query i iff j <= i + offset (causal)
 };
 
@@ -122,8 +133,11 @@ template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const FwdParams prm) {
-  constexpr int LD = HD <= 64 ? 64 : 128;
+  constexpr int LD = HD <= 64 ? 64 : (HD <= 128 ? 128 : 256);
   using Ly = FwdLayout<LD>;
+  constexpr int BK = Ly::BK;       // keys per block
+  constexpr int KC = BK / 2;       // key columns per softmax warp
+  constexpr int kKSt = Ly::kKSt;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_addr(smem);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -166,27 +180,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = qt * kBlk;
   // key blocks this query block sees: all, or (causal) up to the last key its
   // last row sees; none if even that row sees no key
-  int n_blk = prm.nk_tiles;
+  const int nk_blocks = (prm.Nk + BK - 1) / BK;
+  int n_blk = nk_blocks;
   if (prm.causal) {
     const int hi = min(q0 + kBlk - 1, prm.N - 1) + prm.offset;
-    n_blk = hi < 0 ? 0 : min(prm.nk_tiles, hi / kBlk + 1);
+    n_blk = hi < 0 ? 0 : min(nk_blocks, hi / BK + 1);
   }
   const int64_t head = (int64_t)b * prm.sb + (int64_t)h * prm.sh;
   const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
   const uint32_t sQ = sbase + Ly::kQ;
-  auto sK = [&](int st) -> uint32_t { return sbase + Ly::kK + st * Ly::kTile; };
-  auto sV = [&](int st) -> uint32_t { return sbase + Ly::kV + st * Ly::kTile; };
+  auto sK = [&](int st) -> uint32_t { return sbase + Ly::kK + st * Ly::kKVTile; };
+  auto sV = [&](int st) -> uint32_t { return sbase + Ly::kV + st * Ly::kKVTile; };
 
   if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ producers
-    // warp 8: Q once, then K_b into stage b % 3 once S_{b-3} has read it;
+    // warp 8: Q once, then K_b into stage b % kKSt once S_{b-kKSt} has read it;
     // warp 10: V_b into stage b % 2 once O += P_{b-2} V_{b-2} has read it.
     // Each producer waits for its own copies and forwards their completion
     // (K_b to S_READY, V_b to P_FULL), so the MMA warp waits on two
     // barriers per block.  Forwarding block b-1 after issuing block b keeps
     // one copy in flight while the previous one is confirmed.
     const bool isK = warp == 8;
-    const int nst = isK ? kKStages : kVStages;
+    const int nst = isK ? kKSt : kVStages;
     const int full0 = isK ? K_FULL0 : V_FULL0, empty0 = isK ? K_EMPTY0 : V_EMPTY0;
     const CUtensorMap* map = isK ? &tmK : &tmV;
     auto forward = [&](int j) -> bool {
@@ -208,9 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tensormap(map);
       if (isK && n_blk > 0) {
         ptx::prefetch_tensormap(&tmQ);
-        ptx::mbar_arrive_expect_tx(bar(Q_FULL), Ly::kTile);
+        ptx::mbar_arrive_expect_tx(bar(Q_FULL), Ly::kQTile);
 #pragma unroll
-        for (int c = 0; c < LD / 64; ++c) ptx::tma_load_4d(sQ + c * Ly::kChunk, &tmQ, bar(Q_FULL), c * 64, q0, h, b);
+        for (int c = 0; c < LD / 64; ++c) ptx::tma_load_4d(sQ + c * Ly::kQChunk, &tmQ, bar(Q_FULL), c * 64, q0, h, b);
       }
     }
     for (int j = 0; j < n_blk; ++j) {
@@ -218,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j >= nst && !(ok = warp_wait(bar(empty0 + st), ((j - nst) / nst) & 1, W))) break;
       if (lane == 0) {
         const uint32_t dst = isK ? sK(st) : sV(st);
-        ptx::mbar_arrive_expect_tx(bar(full0 + st), Ly::kTile);
+        ptx::mbar_arrive_expect_tx(bar(full0 + st), Ly::kKVTile);
 #pragma unroll
         for (int c = 0; c < LD / 64; ++c)
-          ptx::tma_load_4d(dst + c * Ly::kChunk, map, bar(full0 + st), c * 64, j * kBlk, h, b);
+          ptx::tma_load_4d(dst + c * Ly::kKVChunk, map, bar(full0 + st), c * 64, j * BK, h, b);
       }
       __syncwarp();
       issued = j + 1;
@@ -241,25 +256,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issue
     // order: S_0, S_1, then per block b: S_{b+2}, O += P_b V_b
-    constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, 128, false, false);  // S = Q K^T
-    constexpr uint32_t kIdO = ptx::idesc_bf16_f32(128, HD, false, true);    // O += P V
-    auto kdesc = [&](uint32_t tile, int kk) -> uint64_t {
-      return ptx::sdesc_sw128(tile + (kk >> 2) * Ly::kChunk + (kk & 3) * 32, 16, 1024);
+    constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, BK, false, false);  // S = Q K^T
+    constexpr uint32_t kIdO = ptx::idesc_bf16_f32(128, HD, false, true);   // O += P V
+    auto kdesc = [&](uint32_t tile, uint32_t chunk, int kk) -> uint64_t {
+      return ptx::sdesc_sw128(tile + (kk >> 2) * chunk + (kk & 3) * 32, 16, 1024);
     };
     auto mndesc = [&](uint32_t tile, int kk) -> uint64_t {
-      return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
+      return ptx::sdesc_sw128(tile + kk * 2048, Ly::kKVChunk, 1024);
     };
     const uint32_t tO = tm + Ly::kColO;
     // S_j into buffer j % 3 once K_j has landed and (j >= 3) O += P_{j-3} V_{j-3}
     // has read the buffer
     auto issue_S = [&](int j) -> bool {
-      const int sb = j % kSBufs, ks = j % kKStages;
+      const int sb = j % kSBufs, ks = j % kKSt;
       if (!warp_wait(bar(S_READY0 + sb), (j / kSBufs) & 1, W)) return false;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
-        const uint32_t tS = tm + sb * 128;
+        const uint32_t tS = tm + sb * BK;
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS, kdesc(sQ, kk), kdesc(sK(ks), kk), kIdS, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          ptx::mma_ss(tS, kdesc(sQ, Ly::kQChunk, kk), kdesc(sK(ks), Ly::kKVChunk, kk), kIdS, kk > 0);
         ptx::tc_commit(bar(S_FULL0 + sb));
         ptx::tc_commit(bar(K_EMPTY0 + ks));
       }
@@ -273,14 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_{j+2} first: it only waits for O += P_{j-1} V_{j-1}, so the score
       // block two ahead is in flight while the softmax warps finish P_j
       if (j + 2 < n_blk && !(ok = issue_S(j + 2))) break;
-      // O += P_j V_j  (A = P_j from TMEM: key steps 0-3 in columns [0,32), 4-7 in [64,96))
+      // O += P_j V_j  (A = P_j from TMEM: the 16-key steps of softmax half g in
+      // columns [g KC, g KC + KC/2))
       if (!(ok = warp_wait(bar(P_FULL0 + sb), (j / kSBufs) & 1, W))) break;  // P_j and V_j
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
-        const uint32_t tP = tm + sb * 128;
+        const uint32_t tP = tm + sb * BK;
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          ptx::mma_ts(tO, tP + (kk >> 2) * 64 + (kk & 3) * 8, mndesc(sV(vs), kk), kIdO, (j | kk) != 0);
+        for (int kk = 0; kk < BK / 16; ++kk)
+          ptx::mma_ts(tO, tP + (kk / (KC / 16)) * KC + (kk % (KC / 16)) * 8, mndesc(sV(vs), kk), kIdO, (j | kk) != 0);
         ptx::tc_commit(bar(S_READY0 + sb));  // buffer free for S_{j+3}
         ptx::tc_commit(bar(O_DONE0 + sb));
         ptx::tc_commit(bar(V_EMPTY0 + vs));
@@ -298,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = qq * 32 + lane;          // query row in the block == TMEM lane
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
     const int qrow = q0 + t;
-    const int c0 = G * 64;                 // key columns [c0, c0 + 64) of each block
+    const int c0 = G * KC;                 // key columns [c0, c0 + KC) of each block
     const float sl2 = prm.scale * kLog2e;
     float* xchg = reinterpret_cast<float*>(smem + Ly::kX);
     float m_run = -INFINITY;               // exponent base (log2 units)
@@ -307,25 +324,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_blk; ++j) {
       const int st = j & 1;            // parity of the row-maximum exchange slot
       const int sb = j % kSBufs;       // TMEM buffer of S_j / P_j
-      const uint32_t tS = tm + sb * 128;
+      const uint32_t tS = tm + sb * BK;
       if (!(ok = warp_wait(bar(S_FULL0 + sb), (j / kSBufs) & 1, W))) break;
       ptx::tc_fence_after();
-      uint32_t r[64];
-      ptx::tmem_ld64(tS + lane_off + c0, tS + lane_off + c0 + 32, r);
-      const int k0 = j * kBlk + c0;
-      if ((prm.causal && j * kBlk + kBlk - 1 > q0 + prm.offset) || (j * kBlk + kBlk > prm.Nk)) {
-        // columns c >= lim of this warp's 64 are masked (past N_k, or later
+      uint32_t r[KC];
+      if constexpr (KC == 64)
+        ptx::tmem_ld64(tS + lane_off + c0, tS + lane_off + c0 + 32, *reinterpret_cast<uint32_t(*)[64]>(r));
+      else
+        ptx::tmem_ld32(tS + lane_off + c0, *reinterpret_cast<uint32_t(*)[32]>(r));
+      const int k0 = j * BK + c0;
+      if ((prm.causal && j * BK + BK - 1 > q0 + prm.offset) || (j * BK + BK > prm.Nk)) {
+        // columns c >= lim of this warp's KC are masked (past N_k, or later
         // than the query's last visible key under the causal mask)
         int lim = prm.Nk - k0;
         if (prm.causal) lim = min(lim, qrow + prm.offset - k0 + 1);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) r[c] = c < lim ? r[c] : __float_as_uint(-INFINITY);
+        for (int c = 0; c < KC; ++c) r[c] = c < lim ? r[c] : __float_as_uint(-INFINITY);
       }
       // row maximum of the raw scores (scale > 0 commutes with max), four
       // independent chains
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r[c]));
+      for (int c = 0; c < KC; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r[c]));
       float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
       // row maximum over both halves of the block
       xchg[(st * 2 + G) * kBlk + t] = mx;
@@ -356,16 +376,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m_run = m_new;
       const float mb = m_run == -INFINITY ? 0.f : m_run;
-      uint32_t pk[32];
+      uint32_t pk[KC / 2];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
+      for (int c = 0; c < KC; c += 2) {
         const float p0 = ptx::ex2(fmaf(__uint_as_float(r[c]), sl2, -mb));
         const float p1 = ptx::ex2(fmaf(__uint_as_float(r[c + 1]), sl2, -mb));
         l_part += p0 + p1;
         pk[c / 2] = ptx::pack_bf16x2(p0, p1);
       }
-      ptx::tmem_st16(tS + lane_off + G * 64, &pk[0]);
-      ptx::tmem_st16(tS + lane_off + G * 64 + 16, &pk[16]);
+      // P columns [c0, c0 + KC/2) lie over this warp's own S columns
+#pragma unroll
+      for (int u = 0; u < KC / 32; ++u) ptx::tmem_st16(tS + lane_off + c0 + 16 * u, &pk[16 * u]);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(P_FULL0 + sb));
@@ -424,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD>
 cudaError_t launch_fwd_hd(const fa_problem& p, const CUtensorMap* maps, const FwdParams& prm, cudaStream_t s) {
-  using Ly = FwdLayout<(HD <= 64 ? 64 : 128)>;
+  using Ly = FwdLayout<(HD <= 64 ? 64 : (HD <= 128 ? 128 : 256))>;
   cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
@@ -437,8 +458,9 @@ cudaError_t launch_fwd_hd(const fa_problem& p, const CUtensorMap* maps, const Fw
 cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                              int32_t* status, uint64_t wait_ns, cudaStream_t s) {
   CUtensorMap maps[3];
-  if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
-      !make_bf16_tile_map(&maps[2], V, p, true))
+  const int bk = p.d == 256 ? 64 : kBlk;  // key block rows
+  if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map_rows(&maps[1], K, p, true, bk) ||
+      !make_bf16_tile_map_rows(&maps[2], V, p, true, bk))
     return cudaErrorInvalidValue;
   FwdParams prm;
   prm.O = (__nv_bfloat16*)O;
@@ -450,7 +472,6 @@ cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, 
   prm.N = p.N;
   prm.n_tiles = (int)ceil_div(p.N, kBlk);
   prm.Nk = p.N_k;
-  prm.nk_tiles = (int)ceil_div(p.N_k, kBlk);
   prm.offset = (int)causal_offset(p);
   prm.sb = p.stride_b;
   prm.sh = p.stride_h;
@@ -462,6 +483,7 @@ cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, 
     case 64: return launch_fwd_hd<64>(p, maps, prm, s);
     case 96: return launch_fwd_hd<96>(p, maps, prm, s);
     case 128: return launch_fwd_hd<128>(p, maps, prm, s);
+    case 256: return launch_fwd_hd<256>(p, maps, prm, s);
   }
   return cudaErrorInvalidValue;
 }

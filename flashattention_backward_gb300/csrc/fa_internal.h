@@ -36,15 +36,14 @@ bool normalize_problem(const fa_problem* in, fa_problem* out);  // false: invali
 inline int64_t causal_offset(const fa_problem& p) { return (int64_t)p.N_k - p.N; }
 
 inline bool deterministic(const fa_problem& p) { return (p.flags & FA_FLAG_DETERMINISTIC) != 0; }
-// bf16 with d <= 128 runs on the tensor-core kernels; fp32 on the CUDA-core
-// kernels.  bf16 at d = 256 runs the backward on the tensor cores (two CTAs
-// per key block, one per half of the output columns) and the forward on the
-// CUDA-core kernel (fp32 arithmetic).
-inline bool tensor_core(const fa_problem& p) { return p.dtype == FA_BF16 && p.d <= 128; }
-inline bool tensor_core_bwd(const fa_problem& p) { return p.dtype == FA_BF16 && (p.d <= 128 || p.d == 256); }
+// bf16 runs on the tensor-core kernels (at d = 256 the backward splits each
+// key block over two CTAs, one per half of the output columns); fp32 on the
+// CUDA-core kernels.  The single-launch backward exists for d <= 128.
+inline bool tensor_core(const fa_problem& p) { return p.dtype == FA_BF16; }
+inline bool fused_supported(const fa_problem& p) { return p.dtype == FA_BF16 && p.d <= 128; }
 // Key-block height of the backward kernel that serves p (tensor-core
 // kernels: 128; CUDA-core kernel: 64, or 32 at d = 256).
-inline int key_block_rows(const fa_problem& p) { return tensor_core_bwd(p) ? 128 : (p.d == 256 ? 32 : 64); }
+inline int key_block_rows(const fa_problem& p) { return tensor_core(p) ? 128 : (p.d == 256 ? 32 : 64); }
 // dQ accumulator slices: one per key block in deterministic mode, else one.
 inline int64_t dq_slices(const fa_problem& p) {
   return deterministic(p) ? ceil_div(p.N_k, key_block_rows(p)) : 1;
@@ -58,8 +57,7 @@ inline int64_t dq_slice_elems(const fa_problem& p) {
 cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO, float* D,
                               float* dq_accum, cudaStream_t s);
 cudaError_t launch_convert_dq(const fa_problem& p, const float* dq_accum, void* dQ, cudaStream_t s);
-// CUDA-core forward (fp32, and bf16 at d = 256) and backward (fp32); fp32
-// arithmetic throughout.
+// CUDA-core forward and backward for fp32 problems (exact fp32 arithmetic).
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
                             void* O, float* L, cudaStream_t s);
 cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
@@ -82,7 +80,7 @@ int64_t fused_items(const fa_problem& p);
 cudaError_t launch_bwd_fused_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* O,
                                    const void* dO, const float* L, float* D, float* dq_accum, int32_t* sync,
                                    void* dQ, void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
-// tcgen05 forward for bf16, d in {32, 64, 96, 128}.
+// tcgen05 forward for bf16, d in {32, 64, 96, 128, 256}.
 cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                              int32_t* status, uint64_t wait_ns, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t wait_ns, cudaStream_t s);

@@ -1,7 +1,6 @@
 // CUDA-core (FFMA) kernels for float32 problems (tensor cores have no fp32
 // mode that keeps float32 accuracy, and the fp32 workload is a small
-// correctness problem), and the forward for bf16 at d = 256; inputs are
-// widened to fp32 and all arithmetic is fp32:
+// correctness problem); all arithmetic is fp32:
 //  * the forward pass (online softmax), 64 x 64 tiles;
 //  * the backward pass, 64 x 64 tiles (32 x 32 at d = 256, to fit shared
 //    memory).
@@ -27,9 +26,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float to_f(float x) { return x; }
-__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void from_f(float* p, float v) { *p = v; }
-__device__ __forceinline__ void from_f(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 
 // Copy a ROWS x HD tile of rows [row0, row0 + ROWS) into shared memory as fp32
 // with row pitch `pitch`; rows >= N are zero.
@@ -417,15 +414,10 @@ cudaError_t launch_bwd_dt(const fa_problem& p, const void* Q, const void* K, con
 
 }  // namespace
 
-// Forward: fp32 at every supported d; bf16 only at d = 256 (the tensor-core
-// kernels serve the other bf16 head dims), so only that bf16 instance is
-// built.  Backward: fp32 only (every bf16 head dim has a tensor-core kernel).
+// fp32 only: every bf16 head dim has tensor-core kernels.
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                             cudaStream_t s) {
-  if (p.dtype == FA_BF16)
-    return p.d == 256 ? launch_fwd_t<__nv_bfloat16, 256>(p, (const __nv_bfloat16*)Q, (const __nv_bfloat16*)K,
-                                                         (const __nv_bfloat16*)V, (__nv_bfloat16*)O, L, s)
-                      : cudaErrorInvalidValue;
+  if (p.dtype == FA_BF16) return cudaErrorInvalidValue;
   return launch_fwd_dt<float>(p, Q, K, V, O, L, s);
 }
 

@@ -44,12 +44,11 @@
  *    reductions (the FA2 default; ch.16 §16.3 notes deterministic=False).
  *
  * Supported problems (N is the number of query rows, N_k of key rows; see
- * fa_problem): dtype FA_BF16 with d in {32, 64, 96, 128} (tcgen05
- * tensor-core kernels) or d = 256 (tensor-core backward with each key block
- * split over two CTAs by output columns, since the dK and dV accumulators
- * of one block would fill tensor memory; the forward on a CUDA-core kernel
- * with fp32 arithmetic); dtype FA_FP32 with d in {16, 32, 64, 96, 128, 256}
- * (exact fp32 FFMA kernels, no TF32).  N >= 1, N_k >= 0, B >= 1, H >= 1, N, N_k <= 2^24,
+ * fa_problem): dtype FA_BF16 with d in {32, 64, 96, 128, 256} (tcgen05
+ * tensor-core kernels; at d = 256 the backward splits each key block over
+ * two CTAs by output columns, since the dK and dV accumulators of one block
+ * would fill tensor memory); dtype FA_FP32 with d in {16, 32, 64, 96, 128,
+ * 256} (exact fp32 FFMA kernels, no TF32).  N >= 1, N_k >= 0, B >= 1, H >= 1, N, N_k <= 2^24,
  * B*H <= 2^24.
  * Other d return FA_ERR_UNSUPPORTED.
  *
@@ -178,9 +177,8 @@ fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const v
  * accumulator tile, one key block of the backward, or one query tile's
  * conversion.  Items only wait (bounded) for items with smaller tickets, so
  * the preprocess of the next group of heads and the conversion of the
- * previous one overlap the backward of the current one.  Only problems that
- * run on the tensor-core kernels (bf16, d <= 128); others return
- * FA_ERR_UNSUPPORTED.  D and dQ_accum as for fa_backward; sync: device
+ * previous one overlap the backward of the current one.  Only bf16 problems
+ * with d <= 128; others return FA_ERR_UNSUPPORTED.  D and dQ_accum as for fa_backward; sync: device
  * int32 array of fa_backward_fused_sync_elems(p) elements, scratch owned by
  * the caller (zeroed on `stream` before the launch).  Same results as
  * fa_backward (bitwise with FA_FLAG_DETERMINISTIC). */
