@@ -38,6 +38,8 @@ __all__ = [
     "attention_forward",
     "attention_backward_host",
     "attention_backward",
+    "FlashAttnFunction",
+    "flash_attn_func",
     "get_device_status",
     "set_wait_limit_ns",
     "selftest_wait_timeout",
@@ -309,6 +311,45 @@ def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, st
     else:
         fa_backward(p, q, k, v, o, do, L, D, acc, dq, dk, dv, stream)
     return dq, dk, dv
+
+
+class FlashAttnFunction(torch.autograd.Function):
+    """Autograd node over the library: forward = fa_fwd (O and the row
+    logsumexp L are saved), backward = fa_backward (preprocess, main kernel,
+    convert).  Tensors are [B, H, N, d] (K, V: [B, H, N_k, d]) on a CUDA
+    device, bf16 or fp32, last dimension contiguous; tensors of one shape
+    whose strides differ are passed to the library as dense copies."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal: bool, scale: float, deterministic: bool):
+        if q.stride(-1) != 1:
+            q = q.contiguous()
+        if k.stride(-1) != 1 or v.stride() != k.stride():
+            k, v = k.contiguous(), v.contiguous()
+        o, L = attention_forward(q, k, v, scale, causal)
+        ctx.save_for_backward(q, k, v, o, L)
+        ctx.causal, ctx.scale, ctx.deterministic = causal, scale, deterministic
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, L = ctx.saved_tensors
+        if do.stride() != o.stride():
+            if q.is_contiguous():
+                do = do.contiguous()
+            else:  # the library takes dO with the strides of O
+                do = torch.empty_like(o).copy_(do)
+        dq, dk, dv = attention_backward(q, k, v, o, do, L, ctx.scale, ctx.causal,
+                                        deterministic=ctx.deterministic)
+        return dq, dk, dv, None, None, None
+
+
+def flash_attn_func(q, k, v, causal: bool = False, softmax_scale: Optional[float] = None,
+                    deterministic: bool = False):
+    """O = softmax(softmax_scale Q K^T) V (default scale 1/sqrt(d)), with the
+    FlashAttention-2 backward of this library under autograd."""
+    scale = float(softmax_scale) if softmax_scale is not None else q.shape[-1] ** -0.5
+    return FlashAttnFunction.apply(q, k, v, bool(causal), scale, bool(deterministic))
 
 
 def fa_backward_host_workspace_bytes(p: FaProblem, heads_per_group: int = 0) -> int:
