@@ -1,8 +1,9 @@
 """GPU parity of the tcgen05 bf16 backward against the float64 oracle.
 
 Small problems (ragged tails, causal diagonals, N = 1, d = 64 and 128) are
-compared on every head; the five workloads run at full size in the same
-launch configuration the benchmark times and are compared on sampled heads,
+compared on every head; the bf16 workloads (and the d = 256 one) run at full
+size in the same launch configuration the benchmark times and are compared on
+sampled heads,
 with shape-free properties (finite values, sum_j dK_j = 0,
 sum_j dV_j = sum_i dO_i) checked on every head.  Tolerance: max|dX - ref| /
 max|ref| <= 2e-2 per tensor, L <= 1e-3."""
@@ -106,6 +107,7 @@ WORKLOADS = [
     ("causal", [(0, 0), (0, 21)]),
     ("ragged", [(0, 0), (3, 15)]),
     ("long", [(0, 5)]),
+    ("hd256", [(0, 0), (0, 11)]),
 ]
 
 
