@@ -63,8 +63,6 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "dq_layout.cuh"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -151,14 +149,8 @@ struct D256Params {
   int64_t slice_elems;  // > 0: deterministic, key block kb stores into slice kb
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const ptx::Waiter& w) {
-  return __all_sync(0xffffffffu, ptx::wait_bounded(bar, parity, w, true));
-}
-__device__ __forceinline__ bool warp_wait2(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb, const ptx::Waiter& w) {
-  const bool done = (ptx::mbar_try_wait(a, pa) & ptx::mbar_try_wait(b, pb)) != 0;
-  if (__all_sync(0xffffffffu, done)) return true;
-  return __all_sync(0xffffffffu, ptx::wait_bounded(a, pa, w, true) && ptx::wait_bounded(b, pb, w, true));
-}
+using ptx::warp_wait;
+using ptx::warp_wait2;
 
 // 128 fp32 columns of this thread's TMEM lane -> bf16 in global memory.
 __device__ __forceinline__ void store_row128(uint32_t taddr, bool valid, __nv_bfloat16* dst, float mul) {
@@ -650,43 +642,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-}  // namespace
-
-// [B, H, rows, d] bf16 (Q-shaped: kv = false, K-shaped: kv = true) as a 4-D
-// TMA map with boxes of 64 columns x box_rows rows, 128-byte swizzle; rows
-// past the end and columns past d read as zeros.
-bool make_bf16_tile_map_rows(CUtensorMap* m, const void* base, const fa_problem& p, bool kv, int box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  const int64_t rows = kv ? p.N_k : p.N;
-  const int64_t sn = kv ? p.kstride_n : p.stride_n, sh = kv ? p.kstride_h : p.stride_h;
-  const int64_t sb = kv ? p.kstride_b : p.stride_b;
-  cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)rows, (cuuint64_t)p.H, (cuuint64_t)p.B};
-  cuuint64_t strides[3] = {(cuuint64_t)sn * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-namespace {
-
 template <bool kDet>
 cudaError_t launch_t(const CUtensorMap* maps, const D256Params& prm, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(bwd_d256_kernel<kDet>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
@@ -704,8 +659,10 @@ cudaError_t launch_bwd_d256_sm103(const fa_problem& p, const void* Q, const void
                                   int32_t* status, uint64_t wait_ns, cudaStream_t s) {
   if (p.d != kHD || p.dtype != FA_BF16) return cudaErrorInvalidValue;
   CUtensorMap maps[4];
-  if (!make_bf16_tile_map_rows(&maps[0], Q, p, false, kQRows) || !make_bf16_tile_map_rows(&maps[1], K, p, true, kKeyRows) ||
-      !make_bf16_tile_map_rows(&maps[2], V, p, true, kKeyRows) || !make_bf16_tile_map_rows(&maps[3], dO, p, false, kQRows))
+  if (!make_bf16_tile_map_rows(&maps[0], Q, p, false, kQRows) ||
+      !make_bf16_tile_map_rows(&maps[1], K, p, true, kKeyRows) ||
+      !make_bf16_tile_map_rows(&maps[2], V, p, true, kKeyRows) ||
+      !make_bf16_tile_map_rows(&maps[3], dO, p, false, kQRows))
     return cudaErrorInvalidValue;
   D256Params prm;
   prm.L = L;

@@ -54,7 +54,6 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <mutex>
 #include <type_traits>
 
 #include "dq_layout.cuh"
@@ -150,20 +149,8 @@ struct BwdParams {
   int64_t slice_elems;  // > 0: deterministic, key block kb stores into slice kb
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const ptx::Waiter& w) {
-  // all lanes leave together so that .sync.aligned tcgen05 ops stay converged
-  return __all_sync(0xffffffffu, ptx::wait_bounded(bar, parity, w, true));
-}
-
-// Two barriers at once: both are queried back to back, so when both phases
-// are already complete (the usual case for the second) the warp pays one
-// shared-memory round trip instead of two.
-__device__ __forceinline__ bool warp_wait2(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb,
-                                           const ptx::Waiter& w) {
-  const bool done = (ptx::mbar_try_wait(a, pa) & ptx::mbar_try_wait(b, pb)) != 0;
-  if (__all_sync(0xffffffffu, done)) return true;
-  return __all_sync(0xffffffffu, ptx::wait_bounded(a, pa, w, true) && ptx::wait_bounded(b, pb, w, true));
-}
+using ptx::warp_wait;
+using ptx::warp_wait2;
 
 // NC fp32 columns of this thread's TMEM lane -> bf16 in global (NC a
 // multiple of 16: 32-column pieces, then a 16-column tail).
@@ -950,44 +937,6 @@ cudaError_t launch_fused_d(const CUtensorMap* maps, const BwdParams& prm, const 
               : launch_fused_hd<HD, false, false>(maps, prm, fp, items, s);
 }
 
-}  // namespace
-
-namespace {
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-}  // namespace
-
-// A Q-shaped [B, H, N, d] (kv = false) or K-shaped [B, H, N_k, d] (kv = true)
-// bf16 tensor as a 4-D TMA map with 64 x 128 boxes, 128-byte swizzle; rows
-// past the end and columns past d read as zeros.
-bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p, bool kv) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  const int64_t rows = kv ? p.N_k : p.N;
-  const int64_t sn = kv ? p.kstride_n : p.stride_n, sh = kv ? p.kstride_h : p.stride_h;
-  const int64_t sb = kv ? p.kstride_b : p.stride_b;
-  cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)rows, (cuuint64_t)p.H, (cuuint64_t)p.B};
-  cuuint64_t strides[3] = {(cuuint64_t)sn * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)kBlk, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-namespace {
 // Kernel parameters shared by the separate and the single-launch backward.
 BwdParams bwd_params(const fa_problem& p, const float* L, const float* D, float* dq_accum, void* dK, void* dV,
                      int32_t* status, uint64_t wait_ns) {

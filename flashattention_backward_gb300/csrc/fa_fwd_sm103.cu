@@ -48,9 +48,6 @@
 
 namespace fa {
 
-bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p, bool kv);  // fa_bwd_sm103.cu
-bool make_bf16_tile_map_rows(CUtensorMap* m, const void* base, const fa_problem& p, bool kv,
-                             int box_rows);  // fa_bwd_d256_sm103.cu
 
 namespace {
 
@@ -121,9 +118,7 @@ struct FwdParams {
   int offset;        // Nk - N: key j visible to query i iff j <= i + offset (causal)
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const ptx::Waiter& w) {
-  return __all_sync(0xffffffffu, ptx::wait_bounded(bar, parity, w, true));
-}
+using ptx::warp_wait;
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

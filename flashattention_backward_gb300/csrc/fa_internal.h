@@ -2,6 +2,7 @@
 // Nothing here is part of the public ABI (include/fa.h is).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -52,6 +53,14 @@ inline int64_t dq_slices(const fa_problem& p) {
 inline int64_t dq_slice_elems(const fa_problem& p) {
   return (int64_t)p.B * p.H * ceil_div(p.N, 128) * 128 * p.d;
 }
+
+// A Q-shaped [B, H, N, d] (kv = false) or K-shaped [B, H, N_k, d] (kv = true)
+// bf16 tensor of p as a 4-D TMA map: boxes of 64 columns x box_rows rows,
+// 128-byte swizzle, rows past the end and columns past d read as zeros.
+// False if the map cannot be encoded (or the driver entry point is missing).
+bool make_bf16_tile_map_rows(CUtensorMap* m, const void* base, const fa_problem& p, bool kv, int box_rows);
+// The same with 128-row boxes (the tiles of the head-dim <= 128 kernels).
+bool make_bf16_tile_map(CUtensorMap* m, const void* base, const fa_problem& p, bool kv);
 
 // ---- launchers (return a cudaError_t from the launch) -------------------
 cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO, float* D,

@@ -84,6 +84,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   }
 }
 
+// Warp-wide bounded wait: every lane polls (the warp-wide try_wait measured
+// far faster than one lane polling and broadcasting), and all lanes leave
+// together so that .sync.aligned tcgen05 ops after it stay converged.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Waiter& w) {
+  return __all_sync(0xffffffffu, wait_bounded(bar, parity, w, true));
+}
+
+// Two barriers at once: both are queried back to back, so when both phases
+// are already complete (the usual case for the second) the warp pays one
+// shared-memory round trip instead of two.
+__device__ __forceinline__ bool warp_wait2(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb, const Waiter& w) {
+  const bool done = (mbar_try_wait(a, pa) & mbar_try_wait(b, pb)) != 0;
+  if (__all_sync(0xffffffffu, done)) return true;
+  return __all_sync(0xffffffffu, wait_bounded(a, pa, w, true) && wait_bounded(b, pb, w, true));
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
