@@ -37,14 +37,23 @@ HostPipe* pipe_for_current_device() {
   HostPipe& hp = g_pipe[dev];
   if (hp.ready) return &hp;
   const unsigned f = cudaEventDisableTiming;
-  if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-  if (cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-  if (cudaEventCreateWithFlags(&hp.start, f) != cudaSuccess) return nullptr;
-  if (cudaEventCreateWithFlags(&hp.done, f) != cudaSuccess) return nullptr;
-  for (int s = 0; s < kSlots; ++s) {
-    if (cudaEventCreateWithFlags(&hp.ev_in[s], f) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&hp.ev_comp[s], f) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&hp.ev_out[s], f) != cudaSuccess) return nullptr;
+  bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&hp.start, f) == cudaSuccess && cudaEventCreateWithFlags(&hp.done, f) == cudaSuccess;
+  for (int s = 0; ok && s < kSlots; ++s)
+    ok = cudaEventCreateWithFlags(&hp.ev_in[s], f) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.ev_comp[s], f) == cudaSuccess &&
+         cudaEventCreateWithFlags(&hp.ev_out[s], f) == cudaSuccess;
+  if (!ok) {  // release whatever was created; the next call tries again
+    for (cudaEvent_t* ev : {&hp.start, &hp.done})
+      if (*ev) cudaEventDestroy(*ev);
+    for (int s = 0; s < kSlots; ++s)
+      for (cudaEvent_t ev : {hp.ev_in[s], hp.ev_comp[s], hp.ev_out[s]})
+        if (ev) cudaEventDestroy(ev);
+    if (hp.in) cudaStreamDestroy(hp.in);
+    if (hp.out) cudaStreamDestroy(hp.out);
+    hp = HostPipe();
+    return nullptr;
   }
   hp.ready = true;
   return &hp;
@@ -130,6 +139,7 @@ fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, 
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->start, 0);
   const int groups = (heads + g - 1) / g;
+  fa_status st = FA_OK;
   for (int c = 0; c < groups && e == cudaSuccess; ++c) {
     const int s = c % fa::kSlots;
     const int h0 = c * g;
@@ -161,11 +171,10 @@ fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, 
     pc.kstride_n = pn.d;
     pc.kstride_h = (int64_t)pn.N_k * pn.d;
     pc.kstride_b = (int64_t)gh * pn.N_k * pn.d;
-    fa_status st = fa_backward(&pc, base + lay.q, base + lay.k, base + lay.v, base + lay.o, base + lay.dO,
-                               reinterpret_cast<const float*>(base + lay.L), reinterpret_cast<float*>(base + lay.D),
-                               reinterpret_cast<float*>(base + lay.acc), base + lay.dq, base + lay.dk,
-                               base + lay.dv, cs);
-    if (st != FA_OK) return st;
+    st = fa_backward(&pc, base + lay.q, base + lay.k, base + lay.v, base + lay.o, base + lay.dO,
+                     reinterpret_cast<const float*>(base + lay.L), reinterpret_cast<float*>(base + lay.D),
+                     reinterpret_cast<float*>(base + lay.acc), base + lay.dq, base + lay.dk, base + lay.dv, cs);
+    if (st != FA_OK) break;
     e = cudaEventRecord(hp->ev_comp[s], cs);
     // copy out
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->ev_comp[s], 0);
@@ -176,10 +185,15 @@ fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, 
                           hp->out);
     if (e == cudaSuccess) e = cudaEventRecord(hp->ev_out[s], hp->out);
   }
-  // the caller's stream continues only after the last copy out
-  if (e == cudaSuccess) e = cudaEventRecord(hp->done, hp->out);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, hp->done, 0);
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  // The caller's stream continues only after the last copy out, also when a
+  // group failed, so that no copy of this call is still running when the
+  // caller reuses or frees its buffers.
+  cudaError_t j = cudaEventRecord(hp->done, hp->in);
+  if (j == cudaSuccess) j = cudaStreamWaitEvent(cs, hp->done, 0);
+  if (j == cudaSuccess) j = cudaEventRecord(hp->done, hp->out);
+  if (j == cudaSuccess) j = cudaStreamWaitEvent(cs, hp->done, 0);
+  if (st != FA_OK) return st;
+  return e == cudaSuccess && j == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // extern "C"
