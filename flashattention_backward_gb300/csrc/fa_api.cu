@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <stdint.h>
 #include <stdlib.h>
 
@@ -294,6 +295,9 @@ fa_status validate_normalized(const fa_problem* p) {
   if (!(p->scale == p->scale) || p->scale <= 0.f || p->scale > 1e30f) return FA_ERR_INVALID_ARG;
   if (p->dtype != FA_BF16 && p->dtype != FA_FP32) return FA_ERR_INVALID_ARG;
   if (p->N > (1 << 24) || p->N_k > (1 << 24) || (int64_t)p->B * p->H > (1 << 24)) return FA_ERR_UNSUPPORTED;
+  // every kernel launches a 1-D grid of at most B * H * ceil(rows / 32) * 2 CTAs
+  const int64_t rows = p->N > p->N_k ? p->N : p->N_k;
+  if ((int64_t)p->B * p->H * ((rows + 31) / 32) * 2 > INT32_MAX) return FA_ERR_UNSUPPORTED;
   const int64_t es = p->dtype == FA_BF16 ? 2 : 4;
   if (p->stride_n < p->d || p->stride_h < 1 || p->stride_b < 1) return FA_ERR_INVALID_ARG;
   if ((p->stride_n * es) % 16 || (p->stride_h * es) % 16 || (p->stride_b * es) % 16) return FA_ERR_INVALID_ARG;

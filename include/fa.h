@@ -48,8 +48,9 @@
  * tensor-core kernels; at d = 256 the backward splits each key block over
  * two CTAs by output columns, since the dK and dV accumulators of one block
  * would fill tensor memory); dtype FA_FP32 with d in {16, 32, 64, 96, 128,
- * 256} (exact fp32 FFMA kernels, no TF32).  N >= 1, N_k >= 0, B >= 1, H >= 1, N, N_k <= 2^24,
- * B*H <= 2^24.
+ * 256} (exact fp32 FFMA kernels, no TF32).  N >= 1, N_k >= 0, B >= 1,
+ * H >= 1, N, N_k <= 2^24, B*H <= 2^24, and B*H*ceil(max(N, N_k)/32) < 2^30
+ * (the kernels' 1-D grids).
  * Other d return FA_ERR_UNSUPPORTED.
  *
  * dQ accumulator layout

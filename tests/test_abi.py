@@ -100,6 +100,9 @@ BAD = 0x1000  # a 16-byte aligned dummy address; validation fails before any use
         (dict(N_k=50, kstride_b=2 * 50 * 64, kstride_h=50 * 64, kstride_n=60), fa.FA_ERR_INVALID_ARG),
         (dict(N_k=50, kstride_b=2 * 50 * 64, kstride_h=50 * 64, kstride_n=68), fa.FA_ERR_INVALID_ARG),
         (dict(N_k=(1 << 24) + 1, kstride_b=64, kstride_h=64, kstride_n=64), fa.FA_ERR_UNSUPPORTED),
+        # a 1-D grid of B*H*ceil(rows/32)*2 CTAs would pass 2^31 - 1
+        (dict(B=1 << 10, H=1 << 14, N=1 << 12, stride_b=(1 << 14) * (1 << 12) * 64,
+              stride_h=(1 << 12) * 64, stride_n=64), fa.FA_ERR_UNSUPPORTED),
         (dict(causal=2), fa.FA_ERR_INVALID_ARG),
         (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
         (dict(flags=2), fa.FA_ERR_INVALID_ARG),
