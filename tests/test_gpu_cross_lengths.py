@@ -3,9 +3,8 @@ oracle, through the C ABI.
 
 Covers more keys than queries and more queries than keys (rows that see no
 key: O = 0, L = +inf, zero gradients), one query or one key, ragged tails,
-the tensor-core kernels (bf16; the d = 256 backward too), the CUDA-core
-kernels (fp32, and the bf16 forward at d = 256), deterministic mode and the
-host-tensor pipeline.
+the tensor-core kernels (bf16, d = 256 included), the CUDA-core kernels
+(fp32), deterministic mode and the host-tensor pipeline.
 Tolerances: max|dX - ref| / max|ref| <= 2e-2 for bf16 (L <= 1e-3), 1e-5 for
 fp32 (L <= 1e-6); L = +inf exactly where the oracle has it."""
 

@@ -1,9 +1,9 @@
 """Head dims beyond 64 and 128: GPU parity against the float64 oracle.
 
 bf16 d = 32 and 96 run on the tensor-core kernels (tiles 64 and 128 columns
-wide, the columns past d zero-filled by the TMA); bf16 d = 256 runs the
-backward on the tensor cores (two CTAs per key block, one per half of the
-columns) and the forward on the CUDA-core kernel; fp32 d = 96, 256 run on the
+wide, the columns past d zero-filled by the TMA); bf16 d = 256 runs on the
+tensor cores too (the forward with 64-row key blocks, the backward with two
+CTAs per key block, one per half of the columns); fp32 d = 96, 256 run on the
 CUDA-core kernels (fp32 arithmetic; 32-row key blocks at d = 256).  The
 oracle is the same plain definition at every d.  Tolerances as everywhere:
 max|dX - ref| / max|ref| <= 2e-2 for bf16 (L <= 1e-3), 1e-5 for fp32
