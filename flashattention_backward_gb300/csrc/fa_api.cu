@@ -345,6 +345,7 @@ size_t fa_dq_accum_elems(const fa_problem* p) {
 
 fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* V, void* O, float* L,
                  void* stream) {
+  fa::NvtxRange range("fa_fwd");
   fa_problem pn;
   fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
@@ -358,6 +359,7 @@ fa_status fa_fwd(const fa_problem* p, const void* Q, const void* K, const void* 
 
 fa_status fa_bwd_preprocess(const fa_problem* p, const void* O, const void* dO, float* D, float* dQ_accum,
                             void* stream) {
+  fa::NvtxRange range("fa_bwd_preprocess");
   fa_problem pn;
   fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
@@ -367,6 +369,7 @@ fa_status fa_bwd_preprocess(const fa_problem* p, const void* O, const void* dO, 
 
 fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* V, const void* dO, const float* L,
                  const float* D, float* dQ_accum, void* dK, void* dV, void* stream) {
+  fa::NvtxRange range("fa_bwd");
   fa_problem pn;
   fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
@@ -385,6 +388,7 @@ fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* 
 }
 
 fa_status fa_convert_dq(const fa_problem* p, const float* dQ_accum, void* dQ, void* stream) {
+  fa::NvtxRange range("fa_convert_dq");
   fa_problem pn;
   fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
@@ -395,6 +399,7 @@ fa_status fa_convert_dq(const fa_problem* p, const float* dQ_accum, void* dQ, vo
 fa_status fa_backward(const fa_problem* p, const void* Q, const void* K, const void* V, const void* O,
                       const void* dO, const float* L, float* D, float* dQ_accum, void* dQ, void* dK, void* dV,
                       void* stream) {
+  fa::NvtxRange range("fa_backward");
   fa_problem pn;
   fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;
@@ -415,6 +420,7 @@ size_t fa_backward_fused_sync_elems(const fa_problem* p) {
 fa_status fa_backward_fused(const fa_problem* p, const void* Q, const void* K, const void* V, const void* O,
                             const void* dO, const float* L, float* D, float* dQ_accum, int32_t* sync, void* dQ,
                             void* dK, void* dV, void* stream) {
+  fa::NvtxRange range("fa_backward_fused");
   fa_problem pn;
   fa_status st = normalize(p, &pn);
   if (st != FA_OK) return st;

@@ -112,6 +112,7 @@ size_t fa_backward_host_workspace_bytes(const fa_problem* p, int32_t heads_per_g
 fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, const void* hV, const void* hO,
                            const void* hdO, const float* hL, void* hdQ, void* hdK, void* hdV, void* workspace,
                            size_t workspace_bytes, int32_t heads_per_group, void* stream) {
+  fa::NvtxRange range("fa_backward_host");
   fa_problem pn;
   if (!fa::normalize_problem(p, &pn)) return p ? FA_ERR_UNSUPPORTED : FA_ERR_INVALID_ARG;
   if (!hQ || !hK || !hV || !hO || !hdO || !hL || !hdQ || !hdK || !hdV || !workspace) return FA_ERR_INVALID_ARG;

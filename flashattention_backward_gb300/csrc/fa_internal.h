@@ -4,11 +4,22 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/fa.h"
 
 namespace fa {
+
+// NVTX range around a public entry point, so that Nsight Systems and
+// Nsight Compute timelines show each fa_* call; without a tool attached a
+// push/pop pair costs a few nanoseconds.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Query/key tile height used by the dQ accumulator layout and by the
 // tensor-core kernels.

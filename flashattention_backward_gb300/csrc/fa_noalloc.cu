@@ -69,6 +69,7 @@ bool static_workspace(float** D, float** accum) {
 extern "C" fa_status fa_backward_static_workspace(const fa_problem* p, const void* Q, const void* K, const void* V,
                                                   const void* O, const void* dO, const float* L, void* dQ,
                                                   void* dK, void* dV, void* stream) {
+  fa::NvtxRange range("fa_backward_static_workspace");
   const size_t acc_elems = fa_dq_accum_elems(p);  // 0 when p is NULL or invalid
   if (acc_elems == 0) {
     // report the same code fa_backward's own validation gives; nothing launches
