@@ -412,6 +412,10 @@ def main(argv=None) -> int:
                        "note": "companion forward, not part of the step; 4 B H N^2 d (half if causal)"},
         },
         "clocks": clocks,
+        # ch.16 §16.7's cost model: the backward's 5 GEMMs against the
+        # forward's 2 are 2.5x the FLOPs (the page quotes ~2.9x in time)
+        "bwd_fwd_time_ratio": {"value": bwd_ms / statistics.mean(fwd_ms), "flop_ratio_model": 2.5,
+                               "note": "fa_bwd time / fa_fwd time on this workload"},
     }
     if rank == 0 and not args.no_cpu_baseline:
         tf, dt, sample = oracle_sample_tflops(w, args.cpu_heads)

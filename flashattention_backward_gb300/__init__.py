@@ -31,6 +31,7 @@ __all__ = [
     "fa_fwd",
     "fa_bwd_preprocess",
     "fa_bwd",
+    "fa_bwd_tile_pair_count",
     "fa_convert_dq",
     "fa_backward",
     "fa_backward_host",
@@ -104,6 +105,9 @@ def load_library() -> ctypes.CDLL:
     lib.fa_bwd_preprocess.argtypes = [P, vp, vp, fp, fp, vp]
     lib.fa_bwd.argtypes = [P, vp, vp, vp, vp, fp, fp, fp, vp, vp, vp]
     lib.fa_convert_dq.argtypes = [P, fp, vp, vp]
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.fa_bwd_tile_pair_count.argtypes = [P, vp, vp, vp, vp, fp, fp, fp, vp, vp, vp, i32p, i32p, vp]
+    lib.fa_bwd_tile_pair_count.restype = st
     lib.fa_backward.argtypes = [P, vp, vp, vp, vp, vp, fp, fp, fp, vp, vp, vp, vp]
     for name in ("fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_convert_dq", "fa_backward"):
         getattr(lib, name).restype = st
@@ -249,6 +253,25 @@ def fa_bwd(p: FaProblem, q, k, v, do, L, D, dq_accum, dk, dv, stream=None) -> No
                                  _ptr(dq_accum), _ptr(dk), _ptr(dv), _stream(stream)), "fa_bwd")
 
 
+def fa_bwd_tile_pair_count(p: FaProblem, q, k, v, do, L, D, dq_accum, dk, dv, counts, stream=None):
+    """fa_bwd that also adds the executed (key block, query block) pairs to
+    ``counts[0]`` and those with no visible entry to ``counts[1]`` (``counts``:
+    a zeroed int64 CUDA tensor of 2 elements).  Returns the kernel's block
+    heights (key_rows, query_rows)."""
+    _same_layout(p, q, do)
+    _k_layout(p, k, v, dk, dv)
+    _rows(p, L, D)
+    _accum(p, dq_accum)
+    if counts.dtype != torch.int64 or not counts.is_cuda or counts.numel() < 2:
+        raise ValueError("counts must be an int64 CUDA tensor of 2 elements")
+    kr, qr = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load_library().fa_bwd_tile_pair_count(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(L),
+                                                 _ptr(D), _ptr(dq_accum), _ptr(dk), _ptr(dv), _ptr(counts),
+                                                 ctypes.byref(kr), ctypes.byref(qr), _stream(stream)),
+           "fa_bwd_tile_pair_count")
+    return int(kr.value), int(qr.value)
+
+
 def fa_convert_dq(p: FaProblem, dq_accum, dq, stream=None) -> None:
     _same_layout(p, dq)
     _accum(p, dq_accum)
@@ -293,10 +316,22 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, stream=None):
     return o, L
 
 
+def _raise_on_device_error(stream, what: str) -> None:
+    code = get_device_status(stream)
+    if code != FA_OK:
+        raise FaError(code, what)
+
+
 def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, stream=None, workspace=None,
-                       deterministic: bool = False, fused: bool = False):
+                       deterministic: bool = False, fused: bool = False, check_status: bool = False):
     """dQ, dK, dV.  ``workspace`` may pass preallocated (D, dq_accum) or, with
-    ``fused`` (one kernel launch, tensor-core problems), (D, dq_accum, sync)."""
+    ``fused`` (one kernel launch, tensor-core problems), (D, dq_accum, sync).
+
+    The kernels report device-side errors (a bounded wait that ran out) only
+    through the device status word, and leave their outputs partial in that
+    case.  With ``check_status`` the call synchronises the stream, reads the
+    word and raises :class:`FaError` if it holds an error; otherwise the
+    caller should call :func:`get_device_status` after the step."""
     p = problem_for(q, scale, causal, deterministic, k=k)
     if workspace is None:
         D = torch.empty((p.B, p.H, p.N), dtype=torch.float32, device=q.device)
@@ -310,6 +345,8 @@ def attention_backward(q, k, v, o, do, L, scale: float, causal: bool = False, st
         fa_backward_fused(p, q, k, v, o, do, L, D, acc, sync, dq, dk, dv, stream)
     else:
         fa_backward(p, q, k, v, o, do, L, D, acc, dq, dk, dv, stream)
+    if check_status:
+        _raise_on_device_error(stream, "fa_backward (device)")
     return dq, dk, dv
 
 
@@ -318,17 +355,21 @@ class FlashAttnFunction(torch.autograd.Function):
     logsumexp L are saved), backward = fa_backward (preprocess, main kernel,
     convert).  Tensors are [B, H, N, d] (K, V: [B, H, N_k, d]) on a CUDA
     device, bf16 or fp32, last dimension contiguous; tensors of one shape
-    whose strides differ are passed to the library as dense copies."""
+    whose strides differ are passed to the library as dense copies.  With
+    ``check_status`` both passes read the device status word and raise
+    :class:`FaError` on a device-side error (see :func:`attention_backward`)."""
 
     @staticmethod
-    def forward(ctx, q, k, v, causal: bool, scale: float, deterministic: bool):
+    def forward(ctx, q, k, v, causal: bool, scale: float, deterministic: bool, check_status: bool = False):
         if q.stride(-1) != 1:
             q = q.contiguous()
         if k.stride(-1) != 1 or v.stride() != k.stride():
             k, v = k.contiguous(), v.contiguous()
         o, L = attention_forward(q, k, v, scale, causal)
+        if check_status:
+            _raise_on_device_error(None, "fa_fwd (device)")
         ctx.save_for_backward(q, k, v, o, L)
-        ctx.causal, ctx.scale, ctx.deterministic = causal, scale, deterministic
+        ctx.causal, ctx.scale, ctx.deterministic, ctx.check_status = causal, scale, deterministic, check_status
         return o
 
     @staticmethod
@@ -340,16 +381,21 @@ class FlashAttnFunction(torch.autograd.Function):
             else:  # the library takes dO with the strides of O
                 do = torch.empty_like(o).copy_(do)
         dq, dk, dv = attention_backward(q, k, v, o, do, L, ctx.scale, ctx.causal,
-                                        deterministic=ctx.deterministic)
-        return dq, dk, dv, None, None, None
+                                        deterministic=ctx.deterministic, check_status=ctx.check_status)
+        return dq, dk, dv, None, None, None, None
 
 
 def flash_attn_func(q, k, v, causal: bool = False, softmax_scale: Optional[float] = None,
-                    deterministic: bool = False):
+                    deterministic: bool = False, check_status: bool = False):
     """O = softmax(softmax_scale Q K^T) V (default scale 1/sqrt(d)), with the
-    FlashAttention-2 backward of this library under autograd."""
+    FlashAttention-2 backward of this library under autograd.
+
+    A device-side error (a bounded wait that ran out inside a kernel) is only
+    recorded in the device status word and leaves the outputs partial: pass
+    ``check_status=True`` to have both passes check the word and raise
+    :class:`FaError`, or call :func:`get_device_status` after the step."""
     scale = float(softmax_scale) if softmax_scale is not None else q.shape[-1] ** -0.5
-    return FlashAttnFunction.apply(q, k, v, bool(causal), scale, bool(deterministic))
+    return FlashAttnFunction.apply(q, k, v, bool(causal), scale, bool(deterministic), bool(check_status))
 
 
 def fa_backward_host_workspace_bytes(p: FaProblem, heads_per_group: int = 0) -> int:

@@ -17,8 +17,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libfa.so")
-SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_bwd_sm103.cu", "fa_bwd_d256_sm103.cu", "fa_fwd_sm103.cu", "fa_noalloc.cu",
-           "fa_host.cu", "fa_tma.cu"]
+SOURCES = ["fa_api.cu", "fa_simt.cu", "fa_bwd_sm103.cu", "fa_bwd_sm103_count.cu", "fa_bwd_d256_sm103.cu",
+           "fa_fwd_sm103.cu", "fa_noalloc.cu", "fa_host.cu", "fa_tma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3",

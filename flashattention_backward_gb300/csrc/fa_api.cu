@@ -130,109 +130,101 @@ cudaError_t launch_preprocess(const fa_problem& p, const void* O, const void* dO
 }
 
 // ----------------------------------------------------------------------------
-// Convert: dQ = T(scale * dq_accum), undoing the unit-blocked layout.  One
-// block per (b, h, 128-row tile): a coalesced read of the tile into shared
-// memory (row-major, padded), then row-contiguous 16-byte output stores.
+// Convert: dQ = T(scale * dq_accum), undoing the unit-blocked layout without a
+// trip through shared memory.  A "piece" is 16 columns of one query row: the
+// row's 16 floats of one 2 KB unit, i.e. one float4 in each of the unit's 4
+// column-group planes.  Consecutive threads take consecutive pieces (the
+// column blocks of a row, then the next row), so a warp's loads from one plane
+// are 16-byte pieces of a few contiguous 64-128 byte runs, and its stores
+// cover whole contiguous row segments.  Each thread handles kPieces pieces and
+// issues all their loads before its first store.
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void store_out(float* dst, const float* v, int n) {
-  for (int i = 0; i < n; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+constexpr int kConvThreads = 256;
+constexpr int kConvPieces = 2;
+
+__device__ __forceinline__ void store_piece(float* dst, const float4 (&v)[4], float scale) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    reinterpret_cast<float4*>(dst)[g] = make_float4(scale * v[g].x, scale * v[g].y, scale * v[g].z, scale * v[g].w);
 }
-__device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float* v, int n) {
-  for (int i = 0; i < n; i += 8) {
-    uint4 u;
-    u.x = ptx::pack_bf16x2(v[i], v[i + 1]);
-    u.y = ptx::pack_bf16x2(v[i + 2], v[i + 3]);
-    u.z = ptx::pack_bf16x2(v[i + 4], v[i + 5]);
-    u.w = ptx::pack_bf16x2(v[i + 6], v[i + 7]);
-    *reinterpret_cast<uint4*>(dst + i) = u;
-  }
+__device__ __forceinline__ void store_piece(__nv_bfloat16* dst, const float4 (&v)[4], float scale) {
+  uint4 a, b;
+  a.x = ptx::pack_bf16x2(scale * v[0].x, scale * v[0].y);
+  a.y = ptx::pack_bf16x2(scale * v[0].z, scale * v[0].w);
+  a.z = ptx::pack_bf16x2(scale * v[1].x, scale * v[1].y);
+  a.w = ptx::pack_bf16x2(scale * v[1].z, scale * v[1].w);
+  b.x = ptx::pack_bf16x2(scale * v[2].x, scale * v[2].y);
+  b.y = ptx::pack_bf16x2(scale * v[2].z, scale * v[2].w);
+  b.z = ptx::pack_bf16x2(scale * v[3].x, scale * v[3].y);
+  b.w = ptx::pack_bf16x2(scale * v[3].z, scale * v[3].w);
+  reinterpret_cast<uint4*>(dst)[0] = a;
+  reinterpret_cast<uint4*>(dst)[1] = b;
 }
 
 template <typename T, int HD, bool kSlices>
-__global__ void __launch_bounds__(256) convert_dq_kernel(const float* __restrict__ acc, T* __restrict__ dQ, int H,
-                                                         int N, int64_t sb, int64_t sh, int64_t sn,
-                                                         int tiles_per_head, float scale, int slices,
-                                                         int64_t slice_elems, int causal, int kb_rows,
-                                                         int64_t offset) {
-  constexpr int kPitch = HD + 4;  // floats; keeps 16-byte alignment, staggers banks
-  constexpr int kRows = kTileRows / 2;  // one block per half tile: lane quarters 2 half, 2 half + 1
-  extern __shared__ float4 smem_f4[];
-  float* tile_s = reinterpret_cast<float*>(smem_f4);
-  const int half = blockIdx.x & 1;
-  const int tile = (blockIdx.x >> 1) % tiles_per_head;
-  const int bh = (blockIdx.x >> 1) / tiles_per_head;
-  const int b = bh / H, h = bh % H;
-  const float4* src =
-      reinterpret_cast<const float4*>(acc + dq_unit_offset(bh, tiles_per_head, tile, 2 * half, 0, HD));
-  // Key blocks that touch this query tile: all, or (causal) those starting at
-  // or before the last key its last row sees (row + offset, offset = N_k - N);
-  // none when that is negative.  Their slices are summed in increasing order.
-  int last = slices - 1;
-  if (kSlices && causal) {
-    const int64_t hi = (int64_t)tile * kTileRows + kTileRows - 1 + offset;
-    last = hi < 0 ? -1 : (hi / kb_rows < last ? (int)(hi / kb_rows) : last);
-  }
-  const int64_t slice4 = slice_elems / 4;
-  // a half tile is 2 x (HD/16) units of [4 column groups][32 rows][4 columns];
-  // without slices every load of the thread is issued before the first store
-  constexpr int kLoads = kRows * HD / 4 / 256;
-  if (!kSlices && kLoads * 256 == kRows * HD / 4) {
-    float4 v[kLoads];
+__global__ void __launch_bounds__(kConvThreads) convert_dq_kernel(const float* __restrict__ acc, T* __restrict__ dQ,
+                                                                  int H, int N, int64_t sb, int64_t sh, int64_t sn,
+                                                                  int tiles_per_head, float scale, int slices,
+                                                                  int64_t slice_elems, int causal, int kb_rows,
+                                                                  int64_t offset, int64_t pieces) {
+  constexpr int kCb = HD / 16;  // 16-column blocks (units) per row
+  float4 v[kConvPieces][4];
+  int64_t out_off[kConvPieces];
+  bool live[kConvPieces];
 #pragma unroll
-    for (int j = 0; j < kLoads; ++j) v[j] = __ldg(src + threadIdx.x + j * 256);
-#pragma unroll
-    for (int j = 0; j < kLoads; ++j) {
-      const int k = threadIdx.x + j * 256;
-      const int unit = k / 128, g = (k % 128) / 32, r = k % 32;
-      const int row = (unit / (HD / 16)) * 32 + r, col = (unit % (HD / 16)) * 16 + g * 4;
-      *reinterpret_cast<float4*>(tile_s + row * kPitch + col) = v[j];
+  for (int j = 0; j < kConvPieces; ++j) {
+    const int64_t gp = ((int64_t)blockIdx.x * kConvPieces + j) * kConvThreads + threadIdx.x;
+    const int cb = (int)(gp % kCb);
+    const int64_t rowg = gp / kCb;           // padded row over all heads: (bh * T + tile) * 128 + rt
+    const int rt = (int)(rowg % kTileRows);
+    const int64_t bt = rowg / kTileRows;     // bh * T + tile
+    const int tile = (int)(bt % tiles_per_head);
+    const int64_t bh = bt / tiles_per_head;
+    const int n = tile * kTileRows + rt;
+    live[j] = gp < pieces && n < N;
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    out_off[j] = (int64_t)b * sb + (int64_t)h * sh + (int64_t)n * sn + cb * 16;
+    // the row's float4 in plane g of unit (bt, rt / 32, cb) is at + g * 128
+    const float4* src = reinterpret_cast<const float4*>(acc + ((bt * 4 + rt / 32) * kCb + cb) * 512 + (rt % 32) * 4);
+    // Key blocks that touch this query tile: all, or (causal) those starting
+    // at or before the last key its last row sees (row + offset); none when
+    // that is negative.  Their slices are summed in increasing order.
+    int last = kSlices ? slices - 1 : 0;
+    if (kSlices && causal) {
+      const int64_t hi = (int64_t)tile * kTileRows + kTileRows - 1 + offset;
+      last = hi < 0 ? -1 : (hi / kb_rows < last ? (int)(hi / kb_rows) : last);
     }
-  } else
-#pragma unroll 4
-  for (int k = threadIdx.x; k < kRows * HD / 4; k += 256) {
-    const int unit = k / 128, g = (k % 128) / 32, r = k % 32;
-    const int row = (unit / (HD / 16)) * 32 + r, col = (unit % (HD / 16)) * 16 + g * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (!kSlices || last >= 0) v = __ldg(src + k);
-    if (kSlices)
-      for (int sl = 1; sl <= last; ++sl) {
-        const float4 w = __ldg(src + sl * slice4 + k);
-        v.x += w.x;
-        v.y += w.y;
-        v.z += w.z;
-        v.w += w.w;
-      }
-    *reinterpret_cast<float4*>(tile_s + row * kPitch + col) = v;
-  }
-  __syncthreads();
-  constexpr int kVec = 16 / sizeof(T);           // outputs per 16-byte store
-  constexpr int kPerRow = HD / kVec;
-  for (int k = threadIdx.x; k < kRows * kPerRow; k += 256) {
-    const int r = k / kPerRow, c = (k % kPerRow) * kVec;
-    const int n = tile * kTileRows + half * kRows + r;
-    if (n >= N) continue;
-    float v[kVec];
 #pragma unroll
-    for (int e = 0; e < kVec; ++e) v[e] = scale * tile_s[r * kPitch + c + e];
-    store_out(dQ + (int64_t)b * sb + (int64_t)h * sh + (int64_t)n * sn + c, v, kVec);
+    for (int g = 0; g < 4; ++g) v[j][g] = live[j] && last >= 0 ? __ldg(src + g * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kSlices && live[j]) {
+      const int64_t slice4 = slice_elems / 4;
+      for (int sl = 1; sl <= last; ++sl)
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float4 w = __ldg(src + sl * slice4 + g * 32);
+          v[j][g].x += w.x;
+          v[j][g].y += w.y;
+          v[j][g].z += w.z;
+          v[j][g].w += w.w;
+        }
+    }
   }
+#pragma unroll
+  for (int j = 0; j < kConvPieces; ++j)
+    if (live[j]) store_piece(dQ + out_off[j], v[j], scale);
 }
 
 template <typename T>
 static cudaError_t launch_convert_t(const fa_problem& p, const float* acc, T* dQ, cudaStream_t s) {
   const int tiles = (int)ceil_div(p.N, kTileRows);
-  const dim3 grid((unsigned)((int64_t)p.B * p.H * tiles * 2));
+  const int64_t pieces = (int64_t)p.B * p.H * tiles * kTileRows * (p.d / 16);
+  const dim3 grid((unsigned)ceil_div(pieces, kConvThreads * kConvPieces));
 #define FA_CONV_CASE(HDV)                                                                                  \
   case HDV: {                                                                                              \
-    const size_t sm = (size_t)(kTileRows / 2) * (HDV + 4) * sizeof(float);                                \
     auto kern = deterministic(p) ? convert_dq_kernel<T, HDV, true> : convert_dq_kernel<T, HDV, false>;    \
-    if (sm > 48 * 1024) {                                                                                  \
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);    \
-      if (e != cudaSuccess) return e;                                                                      \
-    }                                                                                                      \
-    kern<<<grid, 256, sm, s>>>(acc, dQ, p.H, p.N, p.stride_b, p.stride_h, p.stride_n, tiles, p.scale,      \
-                               (int)dq_slices(p), dq_slice_elems(p), p.causal, key_block_rows(p),          \
-                               causal_offset(p));                                                          \
+    kern<<<grid, kConvThreads, 0, s>>>(acc, dQ, p.H, p.N, p.stride_b, p.stride_h, p.stride_n, tiles,       \
+                                       p.scale, (int)dq_slices(p), dq_slice_elems(p), p.causal,            \
+                                       key_block_rows(p), causal_offset(p), pieces);                       \
     break;                                                                                                 \
   }
   switch (p.d) {
@@ -385,6 +377,35 @@ fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* 
     return from_cuda(
         fa::launch_bwd_d256_sm103(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s));
   return from_cuda(fa::launch_bwd_sm103(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s));
+}
+
+fa_status fa_bwd_tile_pair_count(const fa_problem* p, const void* Q, const void* K, const void* V, const void* dO,
+                                 const float* L, const float* D, float* dQ_accum, void* dK, void* dV,
+                                 unsigned long long* counts, int32_t* key_rows, int32_t* query_rows, void* stream) {
+  fa::NvtxRange range("fa_bwd_tile_pair_count");
+  fa_problem pn;
+  fa_status st = normalize(p, &pn);
+  if (st != FA_OK) return st;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(L) || !aligned16(D) ||
+      !aligned16(dQ_accum) || !aligned16(dK) || !aligned16(dV) || !counts ||
+      (reinterpret_cast<uintptr_t>(counts) & 7u) || !key_rows || !query_rows)
+    return FA_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!fa::tensor_core(pn)) {
+    *key_rows = *query_rows = fa::key_block_rows(pn);
+    return from_cuda(fa::launch_bwd_simt(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, s, counts));
+  }
+  int32_t* status = fa::device_status_word();
+  if (!status) return FA_ERR_CUDA;
+  *key_rows = 128;
+  if (pn.d == 256) {
+    *query_rows = 64;
+    return from_cuda(fa::launch_bwd_d256_sm103(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(),
+                                               s, counts));
+  }
+  *query_rows = 128;
+  return from_cuda(
+      fa::launch_bwd_sm103_count(pn, Q, K, V, dO, L, D, dQ_accum, dK, dV, status, fa::wait_limit_ns(), s, counts));
 }
 
 fa_status fa_convert_dq(const fa_problem* p, const float* dQ_accum, void* dQ, void* stream) {

@@ -147,6 +147,9 @@ struct D256Params {
   float scale;
   int causal;
   int64_t slice_elems;  // > 0: deterministic, key block kb stores into slice kb
+  // non-null: [0] += (key block, 64-row query block) pairs executed, [1] +=
+  // executed pairs with no visible entry; counted by the column-half-0 CTA
+  unsigned long long* pair_count;
 };
 
 using ptx::warp_wait;
@@ -202,7 +205,9 @@ __device__ __forceinline__ void quad_transpose(float (&x)[4], int b) {
   }
 }
 
-template <bool kDet>
+// kCount: tile-pair accounting into prm.pair_count (instantiated apart, so
+// that the kernel fa_bwd runs carries no counting code).
+template <bool kDet, bool kCount>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -429,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
+    unsigned n_exec = 0, n_masked = 0;  // tile-pair accounting (pair_count)
     for (int i = 0; ok && i < n_iter; ++i) {
       const uint32_t ph = i & 1;
       const uint32_t ph1 = (i + 1) & 1;
@@ -480,6 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_commit(bar(DS_EMPTY));
       }
       __syncwarp();
+      if constexpr (kCount) {
+        const int last_q = min((blk_first + i) * kQRows + kQRows - 1, prm.N - 1);
+        ++n_exec;
+        n_masked += !prm.causal || k0 <= last_q + prm.offset ? 0u : 1u;
+      }
       if (!more) break;
       // dP^T(i+1), each half of the columns as soon as its dO chunks landed
       if (!(ok = warp_wait(bar(DOO_FULL), ph1, W))) break;
@@ -495,7 +506,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-    if (ptx::elect_one()) ptx::tc_commit(bar(ACC_FULL));
+    const bool lead = ptx::elect_one();
+    if (lead) ptx::tc_commit(bar(ACC_FULL));
+    if (kCount && lead && hf == 0) {
+      atomicAdd(prm.pair_count, (unsigned long long)n_exec);
+      atomicAdd(prm.pair_count + 1, (unsigned long long)n_masked);
+    }
     __syncwarp();
     if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
   } else if (warp >= kDrainWarp0) {
@@ -642,13 +658,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kDet>
+template <bool kDet, bool kCount>
 cudaError_t launch_t(const CUtensorMap* maps, const D256Params& prm, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(bwd_d256_kernel<kDet>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(bwd_d256_kernel<kDet, kCount>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
   const int64_t grid = (int64_t)prm.nk_tiles * prm.B * prm.H * 2;
   if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-  bwd_d256_kernel<kDet><<<(unsigned)grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  bwd_d256_kernel<kDet, kCount><<<(unsigned)grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                             prm);
   return cudaGetLastError();
 }
 
@@ -656,7 +674,8 @@ cudaError_t launch_t(const CUtensorMap* maps, const D256Params& prm, cudaStream_
 
 cudaError_t launch_bwd_d256_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
                                   const float* L, const float* D, float* dq_accum, void* dK, void* dV,
-                                  int32_t* status, uint64_t wait_ns, cudaStream_t s) {
+                                  int32_t* status, uint64_t wait_ns, cudaStream_t s,
+                                  unsigned long long* pair_count) {
   if (p.d != kHD || p.dtype != FA_BF16) return cudaErrorInvalidValue;
   CUtensorMap maps[4];
   if (!make_bf16_tile_map_rows(&maps[0], Q, p, false, kQRows) ||
@@ -685,7 +704,9 @@ cudaError_t launch_bwd_d256_sm103(const fa_problem& p, const void* Q, const void
   prm.scale = p.scale;
   prm.causal = p.causal;
   prm.slice_elems = deterministic(p) ? dq_slice_elems(p) : 0;
-  return prm.slice_elems > 0 ? launch_t<true>(maps, prm, s) : launch_t<false>(maps, prm, s);
+  prm.pair_count = pair_count;
+  if (pair_count) return prm.slice_elems > 0 ? launch_t<true, true>(maps, prm, s) : launch_t<false, true>(maps, prm, s);
+  return prm.slice_elems > 0 ? launch_t<true, false>(maps, prm, s) : launch_t<false, false>(maps, prm, s);
 }
 
 }  // namespace fa

@@ -74,7 +74,7 @@ constexpr int kThreads = 32 * (kComputeWarps + kDrainWarps + 2);
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kDrainThreads = 32 * kDrainWarps;
 constexpr int kStagedUnits = 4;                 // dQ units per drain warp staged for one bulk reduction
-constexpr int kHeadGroup = 4;  // heads whose key blocks interleave in the grid order
+constexpr int kHeadGroup = 4;  // heads whose key blocks interleave in the single-launch grid order
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum BarId {
@@ -147,7 +147,18 @@ struct BwdParams {
   float scale;
   int causal;
   int64_t slice_elems;  // > 0: deterministic, key block kb stores into slice kb
+  // non-null: [0] += (key block, query block) pairs executed, [1] += executed
+  // pairs with no visible entry (tile-pair accounting; null in fa_bwd)
+  unsigned long long* pair_count;
+  int head_group;       // heads whose key blocks interleave in the grid order (bwd_sm103_kernel)
 };
+
+// Does query block qb (128 rows) hold a query that sees key k0?  Key j is
+// visible to query i iff j <= i + offset under the causal mask.
+__device__ __forceinline__ bool block_sees_key(int qb, int k0, int N, int offset, int causal) {
+  const int last_q = min(qb * kBlk + kBlk - 1, N - 1);
+  return !causal || k0 <= last_q + offset;
+}
 
 using ptx::warp_wait;
 using ptx::warp_wait2;
@@ -202,7 +213,10 @@ __device__ __forceinline__ bool wait_counter(const int32_t* c, int target, uint6
 // block has reached global memory, add 1 (release).
 // kFused: run inside the single-launch backward (ready and done are used,
 // D is read coherently since this launch writes it); otherwise both are null.
-template <int HD, bool kDet, bool kRect, bool kFused>
+// kCount: tile-pair accounting into prm.pair_count (a separate instantiation,
+// so that the kernels fa_bwd runs carry no counting code: a per-block branch
+// in the MMA warp alone measured 2.6 % slower).
+template <int HD, bool kDet, bool kRect, bool kFused, bool kCount>
 __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                           const CUtensorMap& tmdO, const BwdParams& prm, const int kb, const int bh,
                                           const int32_t* ready, int ready_target, int32_t* done) {
@@ -403,6 +417,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       }
       __syncwarp();
     }
+    unsigned n_exec = 0, n_masked = 0;  // tile-pair accounting (pair_count)
     for (int i = 0; ok && i < n_iter; ++i) {
       const int st = i & 1;
       const int sd = i % kDoSt;
@@ -447,6 +462,10 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         ptx::tc_commit(bar(QEMPTY0 + st));
       }
       __syncwarp();
+      if constexpr (kCount) {
+        ++n_exec;
+        n_masked += block_sees_key(q_first + i, k0, prm.N, prm.offset, prm.causal) ? 0u : 1u;
+      }
       // dP(i+1) once dQ(i) has been drained and dO(i+1) has landed
       if (i + 1 < n_iter) {
         const int sd1 = (i + 1) % kDoSt;
@@ -456,7 +475,12 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         __syncwarp();
       }
     }
-    if (ptx::elect_one()) ptx::tc_commit(bar(ACC_FULL));
+    const bool lead = ptx::elect_one();
+    if (lead) ptx::tc_commit(bar(ACC_FULL));
+    if (kCount && lead) {
+      atomicAdd(prm.pair_count, (unsigned long long)n_exec);
+      atomicAdd(prm.pair_count + 1, (unsigned long long)n_masked);
+    }
     __syncwarp();
     if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
   } else if (warp >= kDrainWarp0) {
@@ -661,22 +685,23 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
   }
 }
 
-template <int HD, bool kDet, bool kRect>
+template <int HD, bool kDet, bool kRect, bool kCount>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                      const BwdParams prm) {
   // work item: key block kb of head (b, h).  Heads are taken in groups of
-  // kHeadGroup so the CTAs resident at any time share a few heads' Q, dO and
-  // dQ accumulator in L2; inside a group the key blocks go round the heads,
-  // key block 0 (the longest causal walk) first, so the short walks of the
-  // last group fill the SMs at the end of the grid.
+  // prm.head_group so the CTAs resident at any time share a few heads' Q, dO
+  // and dQ accumulator in L2; inside a group the key blocks go round the
+  // heads, key block 0 (the longest causal walk) first, so the short walks of
+  // the last group fill the SMs at the end of the grid.
+  const int hg = prm.head_group;
   const int bh_total = prm.B * prm.H;
-  const int grp = blockIdx.x / (kHeadGroup * prm.nk_tiles);
-  const int gsize = min(kHeadGroup, bh_total - grp * kHeadGroup);
-  const int r = blockIdx.x - grp * kHeadGroup * prm.nk_tiles;
-  bwd_block<HD, kDet, kRect, false>(tmQ, tmK, tmV, tmdO, prm, r / gsize, grp * kHeadGroup + r % gsize, nullptr, 0,
-                                    nullptr);
+  const int grp = blockIdx.x / (hg * prm.nk_tiles);
+  const int gsize = min(hg, bh_total - grp * hg);
+  const int r = blockIdx.x - grp * hg * prm.nk_tiles;
+  bwd_block<HD, kDet, kRect, false, kCount>(tmQ, tmK, tmV, tmdO, prm, r / gsize, grp * hg + r % gsize, nullptr, 0,
+                                            nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -889,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Ti = (prm.n_tiles + kTilesPerItem - 1) / kTilesPerItem;  // P and C items per head
   fused_item(ticket, BH, Ti, prm.nk_tiles, role, bh, idx);
   if (role == kItemBwd)
-    bwd_block<HD, kDet, kRect, true>(tmQ, tmK, tmV, tmdO, prm, idx, bh, fp.sync + 1 + bh, Ti,
+    bwd_block<HD, kDet, kRect, true, false>(tmQ, tmK, tmV, tmdO, prm, idx, bh, fp.sync + 1 + bh, Ti,
                                      fp.sync + 1 + BH + bh);
   else if (role == kItemPre)
     pre_item<HD>(prm, fp, bh, idx, !kDet);
@@ -897,22 +922,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     cvt_item<HD, kDet>(prm, fp, smem, bh, idx);
 }
 
-template <int HD, bool kDet, bool kRect>
+template <int HD, bool kDet, bool kRect, bool kCount>
 cudaError_t launch_hd(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t s) {
   using Ly = Layout<(HD <= 64 ? 64 : 128)>;
-  cudaError_t e =
-      cudaFuncSetAttribute(bwd_sm103_kernel<HD, kDet, kRect>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
+  cudaError_t e = cudaFuncSetAttribute(bwd_sm103_kernel<HD, kDet, kRect, kCount>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((int64_t)prm.nk_tiles * p.B * p.H));
-  bwd_sm103_kernel<HD, kDet, kRect><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
+  bwd_sm103_kernel<HD, kDet, kRect, kCount><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3],
+                                                                                prm);
   return cudaGetLastError();
 }
 
-template <int HD>
+template <int HD, bool kCount>
 cudaError_t launch_d(const fa_problem& p, const CUtensorMap* maps, const BwdParams& prm, bool det, bool rect,
                      cudaStream_t s) {
-  if (det) return rect ? launch_hd<HD, true, true>(p, maps, prm, s) : launch_hd<HD, true, false>(p, maps, prm, s);
-  return rect ? launch_hd<HD, false, true>(p, maps, prm, s) : launch_hd<HD, false, false>(p, maps, prm, s);
+  if (det)
+    return rect ? launch_hd<HD, true, true, kCount>(p, maps, prm, s) : launch_hd<HD, true, false, kCount>(p, maps, prm, s);
+  return rect ? launch_hd<HD, false, true, kCount>(p, maps, prm, s) : launch_hd<HD, false, false, kCount>(p, maps, prm, s);
 }
 
 template <int HD, bool kDet, bool kRect>
@@ -937,10 +964,24 @@ cudaError_t launch_fused_d(const CUtensorMap* maps, const BwdParams& prm, const 
               : launch_fused_hd<HD, false, false>(maps, prm, fp, items, s);
 }
 
+// Heads per group of the separate kernel's grid order.  Each key block of a
+// head walks that head's Q and dO blocks and adds into its accumulator tiles,
+// so the group's Q, dO and fp32 accumulator are what the resident CTAs
+// re-read from L2; groups stay within kGroupL2Bytes of them (and at most
+// kHeadGroup heads, which measured best while that fits).
+constexpr int64_t kGroupL2Bytes = int64_t(48) << 20;
+int head_group(const fa_problem& p) {
+  const int64_t per_head = (int64_t)p.N * p.d * 2 * 2 + ceil_div(p.N, kBlk) * kBlk * p.d * 4;
+  const int64_t g = kGroupL2Bytes / per_head;
+  return g < 1 ? 1 : (g > kHeadGroup ? kHeadGroup : (int)g);
+}
+
 // Kernel parameters shared by the separate and the single-launch backward.
 BwdParams bwd_params(const fa_problem& p, const float* L, const float* D, float* dq_accum, void* dK, void* dV,
                      int32_t* status, uint64_t wait_ns) {
   BwdParams prm;
+  prm.pair_count = nullptr;
+  prm.head_group = kHeadGroup;
   prm.L = L;
   prm.D = D;
   prm.dq_accum = dq_accum;
@@ -966,25 +1007,44 @@ BwdParams bwd_params(const fa_problem& p, const float* L, const float* D, float*
   prm.slice_elems = deterministic(p) ? dq_slice_elems(p) : 0;
   return prm;
 }
-}  // namespace
 
-cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
-                             const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
-                             uint64_t wait_ns, cudaStream_t s) {
+// Maps and parameters of one fa_bwd launch, then the kernel for p's head dim.
+template <bool kCount>
+cudaError_t launch_bwd(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
+                       const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
+                       uint64_t wait_ns, cudaStream_t s, unsigned long long* pair_count) {
   CUtensorMap maps[4];
   if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
       !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false))
     return cudaErrorInvalidValue;
   BwdParams prm = bwd_params(p, L, D, dq_accum, dK, dV, status, wait_ns);
+  prm.pair_count = pair_count;
+  prm.head_group = head_group(p);
   const bool det = prm.slice_elems > 0;
   const bool rect = p.causal && prm.offset != 0;
   switch (p.d) {
-    case 32: return launch_d<32>(p, maps, prm, det, rect, s);
-    case 64: return launch_d<64>(p, maps, prm, det, rect, s);
-    case 96: return launch_d<96>(p, maps, prm, det, rect, s);
-    case 128: return launch_d<128>(p, maps, prm, det, rect, s);
+    case 32: return launch_d<32, kCount>(p, maps, prm, det, rect, s);
+    case 64: return launch_d<64, kCount>(p, maps, prm, det, rect, s);
+    case 96: return launch_d<96, kCount>(p, maps, prm, det, rect, s);
+    case 128: return launch_d<128, kCount>(p, maps, prm, det, rect, s);
   }
   return cudaErrorInvalidValue;
+}
+}  // namespace
+
+#if FA_BWD_SM103_COUNTING
+// Built by fa_bwd_sm103_count.cu: the counting instantiations only.
+cudaError_t launch_bwd_sm103_count(const fa_problem& p, const void* Q, const void* K, const void* V,
+                                   const void* dO, const float* L, const float* D, float* dq_accum, void* dK,
+                                   void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s,
+                                   unsigned long long* pair_count) {
+  return launch_bwd<true>(p, Q, K, V, dO, L, D, dq_accum, dK, dV, status, wait_ns, s, pair_count);
+}
+#else
+cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
+                             const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
+                             uint64_t wait_ns, cudaStream_t s) {
+  return launch_bwd<false>(p, Q, K, V, dO, L, D, dq_accum, dK, dV, status, wait_ns, s, nullptr);
 }
 
 int64_t fused_items(const fa_problem& p) {
@@ -1019,5 +1079,7 @@ cudaError_t launch_bwd_fused_sm103(const fa_problem& p, const void* Q, const voi
   }
   return cudaErrorInvalidValue;
 }
+
+#endif  // FA_BWD_SM103_COUNTING
 
 }  // namespace fa

@@ -28,6 +28,10 @@ struct HostPipe {
 };
 std::mutex g_mu;
 HostPipe g_pipe[kMaxDevices];
+// One call at a time per device: the streams and events above are shared, and
+// a second host thread re-recording ev_comp[s] between another call's record
+// and its wait would make that call copy out the wrong group's results.
+std::mutex g_call_mu[kMaxDevices];
 
 // Streams and events are created once per device and reused by every call.
 HostPipe* pipe_for_current_device() {
@@ -129,6 +133,9 @@ fa_status fa_backward_host(const fa_problem* p, const void* hQ, const void* hK, 
     return FA_ERR_INVALID_ARG;
   fa::HostPipe* hp = fa::pipe_for_current_device();
   if (!hp) return FA_ERR_CUDA;
+  // held from the first record to the final join, so that concurrent calls on
+  // one device enqueue one after the other
+  std::lock_guard<std::mutex> call_lock(fa::g_call_mu[hp - fa::g_pipe]);
   cudaStream_t cs = (cudaStream_t)stream;
   const size_t es = pn.dtype == FA_BF16 ? 2 : 4;
   const size_t qhead_bytes = (size_t)pn.N * pn.d * es, khead_bytes = (size_t)pn.N_k * pn.d * es;

@@ -80,19 +80,29 @@ cudaError_t launch_convert_dq(const fa_problem& p, const float* dq_accum, void* 
 // CUDA-core forward and backward for fp32 problems (exact fp32 arithmetic).
 cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
                             void* O, float* L, cudaStream_t s);
+// pair_count (optional, two device words): the backward kernels add the
+// (key block, query block) pairs they execute to [0] and those among them
+// with no visible entry to [1] (tile-pair accounting).
 cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V,
                             const void* dO, const float* L, const float* D, float* dq_accum,
-                            void* dK, void* dV, cudaStream_t s);
+                            void* dK, void* dV, cudaStream_t s, unsigned long long* pair_count = nullptr);
 // tcgen05 / TMEM / TMA backward for bf16, d in {32, 64, 96, 128}.  Returns
 // cudaErrorInvalidValue if a tensor map cannot be encoded.
 cudaError_t launch_bwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V,
                              const void* dO, const float* L, const float* D, float* dq_accum,
                              void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
+// The same with tile-pair accounting into pair_count (instantiations of their
+// own, built in fa_bwd_sm103_count.cu).
+cudaError_t launch_bwd_sm103_count(const fa_problem& p, const void* Q, const void* K, const void* V,
+                                   const void* dO, const float* L, const float* D, float* dq_accum,
+                                   void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s,
+                                   unsigned long long* pair_count);
 // tcgen05 / TMEM / TMA backward for bf16 at d = 256: two CTAs per key block,
 // each accumulating dK and dV for 128 of the 256 columns.
 cudaError_t launch_bwd_d256_sm103(const fa_problem& p, const void* Q, const void* K, const void* V,
                                   const void* dO, const float* L, const float* D, float* dq_accum,
-                                  void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s);
+                                  void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s,
+                                  unsigned long long* pair_count = nullptr);
 // The whole backward (preprocess, tcgen05 backward, convert) in one launch
 // of the tcgen05 kernel for bf16, d in {32, 64, 96, 128}; sync holds
 // 1 + 2 B H int32 (zeroed by the launcher).

@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
     const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
     const float* __restrict__ Lg, const float* __restrict__ Dg, float* __restrict__ dq_accum, T* __restrict__ dK,
     T* __restrict__ dV, int H, int N, int64_t sb, int64_t sh, int64_t sn, float scale, int causal,
-    int64_t slice_elems, int Nk, int64_t ksb, int64_t ksh, int64_t ksn) {
+    int64_t slice_elems, int Nk, int64_t ksb, int64_t ksh, int64_t ksn, unsigned long long* pair_count) {
   // slice_elems > 0 (deterministic): this key block's dQ contributions are
   // stored into its own slice of the accumulator instead of added.
   // Q, dO: N rows with strides (sb, sh, sn); K, V, dK, dV: Nk rows with
@@ -229,8 +229,13 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
 
   // first query tile holding a query that sees key k0: i >= k0 - offset
   const int qt_first = causal && k0 > offset ? (k0 - offset) / KT : 0;
+  unsigned n_exec = 0, n_masked = 0;  // tile-pair accounting (pair_count)
   for (int qt = qt_first; qt < tiles; ++qt) {
     const int q0 = qt * KT;
+    if (pair_count) {
+      ++n_exec;
+      n_masked += !causal || k0 <= min(q0 + KT - 1, N - 1) + offset ? 0u : 1u;
+    }
     __syncthreads();
     load_tile<T, HD, KT>(sQ, kP, Q + head, sn, q0, N);
     load_tile<T, HD, KT>(sdO, kP, dO + head, sn, q0, N);
@@ -332,6 +337,10 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(
       }
     }
   }
+  if (pair_count && threadIdx.x == 0) {
+    atomicAdd(pair_count, (unsigned long long)n_exec);
+    atomicAdd(pair_count + 1, (unsigned long long)n_masked);
+  }
 #pragma unroll
   for (int a = 0; a < kR; ++a) {
     const int j = k0 + ty + 16 * a;
@@ -384,7 +393,8 @@ cudaError_t launch_fwd_dt(const fa_problem& p, const void* Q, const void* K, con
 
 template <typename T, int HD>
 cudaError_t launch_bwd_t(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
-                         const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s) {
+                         const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s,
+                         unsigned long long* pc) {
   constexpr int KT = HD == 256 ? 32 : kT;
   const size_t sm = sizeof(float) * (size_t)(4 * KT * (HD + 1) + 2 * KT * (KT + 1) + 2 * KT);
   cudaError_t e = set_smem(bwd_simt_kernel<T, HD, KT>, sm);
@@ -394,20 +404,21 @@ cudaError_t launch_bwd_t(const fa_problem& p, const void* Q, const void* K, cons
   bwd_simt_kernel<T, HD, KT><<<grid, kThreads, sm, s>>>(
       (const T*)Q, (const T*)K, (const T*)V, (const T*)dO, L, D, acc, (T*)dK, (T*)dV, p.H, p.N, p.stride_b,
       p.stride_h, p.stride_n, p.scale, p.causal, deterministic(p) ? dq_slice_elems(p) : 0, p.N_k, p.kstride_b,
-      p.kstride_h, p.kstride_n);
+      p.kstride_h, p.kstride_n, pc);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_bwd_dt(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
-                          const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s) {
+                          const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s,
+                          unsigned long long* pc) {
   switch (p.d) {
-    case 16: return launch_bwd_t<T, 16>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-    case 32: return launch_bwd_t<T, 32>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-    case 64: return launch_bwd_t<T, 64>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-    case 96: return launch_bwd_t<T, 96>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-    case 128: return launch_bwd_t<T, 128>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
-    case 256: return launch_bwd_t<T, 256>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
+    case 16: return launch_bwd_t<T, 16>(p, Q, K, V, dO, L, D, acc, dK, dV, s, pc);
+    case 32: return launch_bwd_t<T, 32>(p, Q, K, V, dO, L, D, acc, dK, dV, s, pc);
+    case 64: return launch_bwd_t<T, 64>(p, Q, K, V, dO, L, D, acc, dK, dV, s, pc);
+    case 96: return launch_bwd_t<T, 96>(p, Q, K, V, dO, L, D, acc, dK, dV, s, pc);
+    case 128: return launch_bwd_t<T, 128>(p, Q, K, V, dO, L, D, acc, dK, dV, s, pc);
+    case 256: return launch_bwd_t<T, 256>(p, Q, K, V, dO, L, D, acc, dK, dV, s, pc);
   }
   return cudaErrorInvalidValue;
 }
@@ -422,9 +433,10 @@ cudaError_t launch_fwd_simt(const fa_problem& p, const void* Q, const void* K, c
 }
 
 cudaError_t launch_bwd_simt(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
-                            const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s) {
+                            const float* L, const float* D, float* acc, void* dK, void* dV, cudaStream_t s,
+                            unsigned long long* pair_count) {
   if (p.dtype == FA_BF16) return cudaErrorInvalidValue;
-  return launch_bwd_dt<float>(p, Q, K, V, dO, L, D, acc, dK, dV, s);
+  return launch_bwd_dt<float>(p, Q, K, V, dO, L, D, acc, dK, dV, s, pair_count);
 }
 
 }  // namespace fa

@@ -160,6 +160,27 @@ fa_status fa_bwd(const fa_problem* p, const void* Q, const void* K, const void* 
                  const void* dO, const float* L, const float* D, float* dQ_accum,
                  void* dK, void* dV, void* stream);
 
+/* fa_bwd with tile-pair accounting, to check the causal skip on the device
+ * (CS349E lecture 11 demo 4: a causal backward over T x T square blocks needs
+ * only the T(T+1)/2 pairs that hold a visible entry, a fraction 1/2 + 1/(2T);
+ * ch.16 §16.8 item 2: fully masked tiles are neither loaded nor computed).
+ * Same arguments and results as fa_bwd, plus:
+ *   counts      device array of two unsigned 64-bit words, 8-byte aligned,
+ *               owned and zeroed by the caller; the kernel adds the number of
+ *               (key block, query block) pairs it executed to counts[0] and
+ *               the number of those with no visible entry to counts[1]
+ *   key_rows, query_rows   host int32, set before the launch to the block
+ *               heights of the kernel that runs: 128 x 128 for bf16 with
+ *               d <= 128; 128 keys x 64 queries at d = 256 (the two
+ *               column-half CTAs of a key block execute each pair, which is
+ *               counted once); 64 x 64 for fp32 (32 x 32 at d = 256).
+ * The counting costs one register update per pair in the MMA-issuing warp;
+ * fa_bwd runs the same kernels with counting off. */
+fa_status fa_bwd_tile_pair_count(const fa_problem* p, const void* Q, const void* K, const void* V,
+                                 const void* dO, const float* L, const float* D, float* dQ_accum,
+                                 void* dK, void* dV, unsigned long long* counts, int32_t* key_rows,
+                                 int32_t* query_rows, void* stream);
+
 /* dQ = dtype(scale * dQ_accum) (ch.16 §16.3: the convert kernel applies the
  * softmax scale and casts; with FA_FLAG_DETERMINISTIC it first sums the key
  * blocks' slices in increasing order).  Reads dQ_accum, writes dQ. */
@@ -199,7 +220,9 @@ fa_status fa_backward_fused(const fa_problem* p, const void* Q, const void* K, c
  * copied in and group c-1 copied out while group c runs fa_backward on
  * `stream`.  Returns after enqueueing; `stream` continues only once the last
  * result has reached host memory.  Copies use two library-owned streams
- * created on first use per device.  No counterpart on the pages: it feeds
+ * created on first use per device; concurrent calls on one device (from
+ * several host threads) take a per-device lock and enqueue one after the
+ * other, so each gets its own results.  No counterpart on the pages: it feeds
  * the backward from host-resident activations. */
 size_t fa_backward_host_workspace_bytes(const fa_problem* p, int32_t heads_per_group);
 fa_status fa_backward_host(const fa_problem* p, const void* Q, const void* K, const void* V, const void* O,

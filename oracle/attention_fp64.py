@@ -264,17 +264,23 @@ def attention_loss(Q, K, V, G, scale: float, causal: bool = False) -> float:
     return float(np.sum(O * _as4d(G)))
 
 
-def causal_executed_tile_pairs(N: int, Br: int, Bc: int) -> int:
+def causal_executed_tile_pairs(N: int, Br: int, Bc: int, N_k: int | None = None, causal: bool = True) -> int:
     """Number of (key block, query block) pairs that hold at least one visible
-    (j <= i) entry, counted by brute force over the blocks.  CS349E lecture 11
-    demo 4 gives T(T+1)/2 for square blocks."""
+    entry, counted by brute force over the blocks: query blocks of Br rows,
+    key blocks of Bc rows.  Under the causal mask key j is visible to query i
+    iff j <= i + (N_k - N) (N_k defaults to N, the pages' case); a pair is
+    live iff its first key is visible to its last query.  Without the mask
+    every pair is live.  CS349E lecture 11 demo 4 gives T(T+1)/2 for square
+    blocks and N_k = N."""
+    Nk = N if N_k is None else N_k
+    offset = Nk - N
     tq = -(-N // Br)
-    tk = -(-N // Bc)
+    tk = -(-Nk // Bc)
     count = 0
     for kb in range(tk):
         j0 = kb * Bc
         for qb in range(tq):
             i1 = min(N, (qb + 1) * Br) - 1
-            if j0 <= i1:
+            if not causal or j0 <= i1 + offset:
                 count += 1
     return count

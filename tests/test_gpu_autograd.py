@@ -75,3 +75,25 @@ def test_autograd_deterministic_is_bitwise_repeatable():
     assert fa.get_device_status() == 0
     for a, b in zip(*grads):
         assert torch.equal(a, b)
+
+
+def test_check_status_raises_on_a_recorded_device_error():
+    """A device-side error only reaches the status word; with check_status the
+    Python layer reads it after the step and raises.  The error is planted by
+    the library's bounded-wait self test (a barrier nothing arrives at), so no
+    kernel of the backward itself has to fail."""
+    gen = torch.Generator().manual_seed(9)
+    q, k, v = (torch.randn(1, 2, 256, 64, generator=gen).to(torch.bfloat16).to(DEV) for _ in range(3))
+    ql, kl, vl = _leaf(q), _leaf(k), _leaf(v)
+    o = fa.flash_attn_func(ql, kl, vl, causal=True, check_status=True)  # clean: no raise
+    fa.selftest_wait_timeout(5_000_000)  # records FA_ERR_TIMEOUT after 5 ms
+    with pytest.raises(fa.FaError) as err:
+        o.float().sum().backward()
+    assert err.value.code == fa.FA_ERR_TIMEOUT
+    assert fa.get_device_status() == 0  # the read cleared the word
+    o2, L = fa.attention_forward(q, k, v, 0.125, True)
+    fa.selftest_wait_timeout(5_000_000)
+    with pytest.raises(fa.FaError):
+        fa.attention_backward(q, k, v, o2, o2, L, 0.125, True, check_status=True)
+    dq, dk, dv = fa.attention_backward(q, k, v, o2, o2, L, 0.125, True, check_status=True)
+    assert torch.isfinite(dq.float()).all()

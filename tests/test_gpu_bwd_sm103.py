@@ -1,12 +1,19 @@
 """GPU parity of the tcgen05 bf16 backward against the float64 oracle.
 
-Small problems (ragged tails, causal diagonals, N = 1, d = 64 and 128) are
-compared on every head; the bf16 workloads (and the d = 256 one) run at full
-size in the same launch configuration the benchmark times and are compared on
-sampled heads,
-with shape-free properties (finite values, sum_j dK_j = 0,
-sum_j dV_j = sum_i dO_i) checked on every head.  Tolerance: max|dX - ref| /
-max|ref| <= 2e-2 per tensor, L <= 1e-3."""
+Small problems (ragged tails, causal diagonals, N = 1, d = 64 and 128) and
+the bf16 workloads at full size (in the launch configuration the benchmark
+times, the d = 256 one included) are compared with the oracle element by
+element on every head.  The full-size oracle runs one head per task in a
+spawn pool (``oracle_pool``).  Shape-free properties (finite values,
+sum_j dK_j = 0, sum_j dV_j = sum_i dO_i) are checked as well.  Tolerance:
+max|dX - ref| / max|ref| <= 2e-2 per tensor (here per head, which is
+stricter than over the whole tensor), L <= 1e-3.
+
+With FA_PARITY_LOG set to a file name, each full-size workload appends one
+JSON line with its whole-tensor and worst per-head ratios."""
+
+import json
+import os
 
 import numpy as np
 import pytest
@@ -15,6 +22,7 @@ import torch
 import flashattention_backward_gb300 as fa
 from fa_inputs import to_f64, workload
 from gpu_common import compare_head, run_gpu
+from oracle_pool import TENSORS, run_heads, summarize
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -102,20 +110,32 @@ def _properties(out, w):
     assert np.abs(lhs - rhs).max() <= TOL * np.abs(rhs).max()
 
 
-WORKLOADS = [
-    ("mha", [(0, 0), (0, 17), (0, 31)]),
-    ("causal", [(0, 0), (0, 21)]),
-    ("ragged", [(0, 0), (3, 15)]),
-    ("long", [(0, 5)]),
-    ("hd256", [(0, 0), (0, 11)]),
-]
+FULL_SIZE = ["mha", "causal", "ragged", "long", "hd256"]
 
 
-@pytest.mark.parametrize("name,heads", WORKLOADS, ids=[w[0] for w in WORKLOADS])
-def test_workload_full_size(name, heads):
+def _head_tasks(out, w):
+    f32 = lambda t: t.float().numpy()
+    keys = dict(O="o", L="L", dQ="dq", dK="dk", dV="dv")
+    for b in range(w.B):
+        for h in range(w.H):
+            yield (f32(out["q"][b, h]), f32(out["k"][b, h]), f32(out["v"][b, h]), f32(out["g"][b, h]), w.scale,
+                   w.causal, {n: f32(out[keys[n]][b, h]) for n in TENSORS})
+
+
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_workload_full_size(name):
     w = workload(name)
     out = run_gpu(w, DEV)
     assert out["status"] == 0
     _properties(out, w)
-    for b, h in heads:
-        compare_head(out, w, b, h, TOL)
+    per_head = run_heads(list(_head_tasks(out, w)))
+    assert len(per_head) == w.B * w.H
+    for i, e in enumerate(per_head):
+        assert all(e[n][2] for n in TENSORS), f"non-finite output in head {i}"
+    whole, worst = summarize(per_head)
+    log = os.environ.get("FA_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"workload": name, "heads": len(per_head), "whole": whole, "worst_head": worst}) + "\n")
+    bad = {n: r for n, r in worst.items() if r > (1e-3 if n == "L" else TOL)}
+    assert not bad, f"{name}: worst per-head ratios {worst}"

@@ -69,3 +69,53 @@ def test_host_pipeline_rejects_strided_host_tensors():
     r = lib.fa_backward_host(ctypes.byref(p), *([q.data_ptr()] * 6), *([q.data_ptr()] * 3), ws.data_ptr(),
                              ws.numel(), 0, None)
     assert r == fa.FA_ERR_INVALID_ARG
+
+
+def test_host_pipeline_concurrent_threads():
+    """Two host threads call fa_backward_host on one device at once, each on
+    its own stream with its own inputs.  The library's streams and events are
+    shared per device, so the calls must enqueue one after the other; each
+    result must equal (bitwise, deterministic mode) the same call made alone."""
+    import threading
+
+    cases = []
+    for seed in (61, 62):
+        w = workload("causal", B=2, H=5, N=700, d=128, seed=seed)
+        q, k, v, o, g, L = _forward(w)
+        p = fa.problem_for(q, w.scale, True, True)
+        ws = torch.empty(fa.fa_backward_host_workspace_bytes(p, 2), dtype=torch.uint8, device=DEV)
+        out = tuple(torch.empty_like(t).pin_memory() for t in (q, k, v))
+        cases.append(dict(w=w, args=(q, k, v, o, g, L), ws=ws, out=out, stream=torch.cuda.Stream()))
+    alone = []
+    for c in cases:
+        res = fa.attention_backward_host(*c["args"], c["w"].scale, True, 2, workspace=c["ws"], out=c["out"],
+                                         stream=c["stream"], deterministic=True)
+        c["stream"].synchronize()
+        alone.append(tuple(t.clone() for t in res))
+    assert fa.get_device_status() == 0
+    errors = []
+
+    def worker(i):
+        c = cases[i]
+        try:
+            torch.cuda.set_device(0)
+            for _ in range(6):
+                for t in c["out"]:
+                    t.fill_(float("nan"))
+                res = fa.attention_backward_host(*c["args"], c["w"].scale, True, 2, workspace=c["ws"], out=c["out"],
+                                                 stream=c["stream"], deterministic=True)
+                c["stream"].synchronize()
+                for x, y in zip(res, alone[i]):
+                    if not torch.equal(x, y):
+                        errors.append(f"thread {i}: result differs from the call made alone")
+                        return
+        except Exception as e:  # reported below, in the test's own thread
+            errors.append(f"thread {i}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert fa.get_device_status() == 0

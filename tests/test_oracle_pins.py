@@ -301,3 +301,30 @@ def test_workload_shapes_match_page_sizes():
     assert w.B * w.H * w.N * w.d * 2 == gold["Q_bytes"]
     assert w.B * w.H * w.N * w.N * 2 == gold["S_bf16_bytes"]
     assert w.B * w.H * w.N * 4 == gold["L_fp32_bytes"]
+
+
+def _live_pairs_by_elements(N, Nk, Br, Bc, causal):
+    """Brute force over every (query, key) entry: a block pair is live iff
+    some entry in it is visible (j <= i + Nk - N under the causal mask)."""
+    i = np.arange(N)[:, None]
+    j = np.arange(Nk)[None, :]
+    vis = (j <= i + (Nk - N)) if causal else np.ones((N, Nk), dtype=bool)
+    count = 0
+    for q0 in range(0, N, Br):
+        for k0 in range(0, Nk, Bc):
+            count += bool(vis[q0:q0 + Br, k0:k0 + Bc].any())
+    return count
+
+
+@pytest.mark.parametrize("N,Nk,Br,Bc", [(300, 300, 64, 64), (200, 330, 128, 128), (330, 200, 128, 128),
+                                         (1000, 777, 128, 128), (257, 129, 64, 128), (50, 700, 32, 64),
+                                         (700, 50, 64, 32), (128, 128, 128, 128)])
+@pytest.mark.parametrize("causal", [True, False])
+def test_executed_pairs_match_element_brute_force(N, Nk, Br, Bc, causal):
+    """The block-level count (first key visible to the last query) equals a
+    brute force over the mask's entries, for N_q != N_k, ragged tails and
+    unequal block heights; without the mask every pair counts."""
+    got = causal_executed_tile_pairs(N, Br, Bc, N_k=Nk, causal=causal)
+    assert got == _live_pairs_by_elements(N, Nk, Br, Bc, causal)
+    if not causal:
+        assert got == (-(-N // Br)) * (-(-Nk // Bc))
