@@ -14,7 +14,7 @@
 // what dV += P^T dO and dK += dS^T Q need, and P^T feeds the dV product
 // straight from tensor memory.
 //
-// Warp roles (704 threads):
+// Warp roles (736 threads):
 //   warps 0-15 compute.  Warp w owns TMEM lanes 32*(w%4) .. +31 (key rows for
 //              S, dP, dV, dK) and column quarter w/4 of them (four warps per
 //              SM sub-partition hide each other's latencies).
@@ -27,7 +27,10 @@
 //              accumulator, off the compute warps' path.
 //   warp 20    TMA producer: K, V once; Q (two stages, with its L and D rows)
 //              and dO (one stage for d = 128, two for d = 64).
-//   warp 21    TMEM allocator and MMA issuer (one elected lane issues).
+//   warp 21    TMEM allocator; issues dV(i) and S(i+1).
+//   warp 22    issues dQ(i), dK(i) and dP(i+1).  Each MMA warp waits only on
+//              its own chain's barriers, so one's waits overlap the other's
+//              issue (one elected lane of each issues).
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128)     S^T; P^T (bf16) is written over it: query columns
@@ -36,8 +39,9 @@
 //   [256,256+d) dV accumulator, [256+LD,256+LD+d) dK accumulator (LD = 64
 //               for d <= 64, else 128)
 //
-// MMA issue order per query block i (software pipelined):
-//   dV(i)  S(i+1)  dQ(i)  dK(i)  dP(i+1)
+// MMA issue order per query block i (software pipelined), per MMA warp:
+//   warp 21:  dV(i)  S(i+1)
+//   warp 22:  dQ(i)  dK(i)  dP(i+1)
 // dQ goes first so that its drain starts early, and dP(i+1) is issued as soon
 // as the drain warps have read dQ(i) out of the columns dP shares, so the
 // tensor pipe computes dP(i+1) while the compute warps turn S(i+1) into
@@ -69,8 +73,9 @@ constexpr int kComputeWarps = 16;               // 4 per TMEM lane quarter
 constexpr int kDrainWarps = 4;                  // 1 per TMEM lane quarter
 constexpr int kDrainWarp0 = kComputeWarps;      // warps 16-19
 constexpr int kProducerWarp = kComputeWarps + kDrainWarps;
-constexpr int kMmaWarp = kProducerWarp + 1;     // on the same SM sub-partition as lane quarter 1
-constexpr int kThreads = 32 * (kComputeWarps + kDrainWarps + 2);
+constexpr int kMmaWarp = kProducerWarp + 1;     // dV and S^T; TMEM allocator
+constexpr int kMma2Warp = kMmaWarp + 1;         // dQ, dK and dP^T
+constexpr int kThreads = 32 * (kComputeWarps + kDrainWarps + 3);
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kDrainThreads = 32 * kDrainWarps;
 constexpr int kStagedUnits = 4;                 // dQ units per drain warp staged for one bulk reduction
@@ -242,8 +247,8 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     ptx::mbar_init(bar(QEMPTY1), 1);
     ptx::mbar_init(bar(DOFULL0), 1);
     ptx::mbar_init(bar(DOFULL1), 1);
-    ptx::mbar_init(bar(DOEMPTY0), 1);
-    ptx::mbar_init(bar(DOEMPTY1), 1);
+    ptx::mbar_init(bar(DOEMPTY0), 2);  // dP (second MMA warp) and dV (first) read the stage
+    ptx::mbar_init(bar(DOEMPTY1), 2);
     ptx::mbar_init(bar(S_FULL0), 1);
     ptx::mbar_init(bar(S_FULL1), 1);
     ptx::mbar_init(bar(P_FULL), kComputeThreads);
@@ -252,7 +257,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     ptx::mbar_init(bar(DS_FULL), kComputeThreads);
     ptx::mbar_init(bar(DQ_FULL), 1);
     ptx::mbar_init(bar(DQ_EMPTY), kDrainThreads);
-    ptx::mbar_init(bar(ACC_FULL), 1);
+    ptx::mbar_init(bar(ACC_FULL), 2);  // one commit from each MMA warp
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -371,12 +376,19 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       for (int i = do_issued > kDoSt ? do_issued - kDoSt : 0; i < do_issued; ++i)
         ptx::wait_bounded(bar(DOFULL0 + i % kDoSt), (i / kDoSt) & 1, W, false);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMma2Warp) {
     // ------------------------------------------------------------ MMA issue
-    // The whole warp runs this loop and waits; one elected lane issues the
-    // MMAs and commits.  Every operand is warp-uniform (the TMEM base is
-    // broadcast from lane 0, K steps are unrolled) so each tcgen05.mma issues
-    // at the tensor pipe's own rate.
+    // Two warps issue, each running its own chain (disjoint accumulators and
+    // operand buffers), so that one warp's barrier waits overlap the other's:
+    //   first  (kMmaWarp):  dV(i) once P(i) is in TMEM, then S(i+1)
+    //   second (kMma2Warp): dQ(i), dK(i) once dS(i) is in shared memory, then
+    //                       dP(i+1) once the drain has read dQ(i) out of the
+    //                       columns dP shares
+    // A dO stage is released by both (dV and dP read it).  The whole warp
+    // runs each loop and waits; one elected lane issues the MMAs and commits.
+    // Every operand is warp-uniform (the TMEM base is broadcast from lane 0,
+    // K steps are unrolled) so each tcgen05.mma issues at the tensor pipe's
+    // own rate.
     constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
     constexpr uint32_t kIdKV = ptx::idesc_bf16_f32(128, HD, false, true);   // dV, dK
     constexpr uint32_t kIdQ = ptx::idesc_bf16_f32(128, HD, true, true);     // dQ
@@ -398,91 +410,103 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS(i), kdesc(sK, kk), kdesc(sQ(i & 1), kk), kIdS, kk > 0);
       ptx::tc_commit(bar(S_FULL0 + (kSB == 2 ? (i & 1) : 0)));
     };
-
-    // dP^T = V dO^T into the columns that held dQ of the previous block
+    // dP^T = V dO^T into the columns that held dQ of the previous block; the
+    // dO stage's dP reader is done at this commit
     auto issue_dP = [&](int sd) {
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tdP, kdesc(sV, kk), kdesc(sdO(sd), kk), kIdS, kk > 0);
       ptx::tc_commit(bar(DP_FULL));
+      ptx::tc_commit(bar(DOEMPTY0 + sd));
     };
 
-    // Per query block i: dV(i), S(i+1), dQ(i), dK(i), then dP(i+1) as soon
-    // as the drain warps have read dQ(i) out of the columns dP shares.
-    bool ok = warp_wait(bar(KV_FULL), 0, W) && warp_wait2(bar(QFULL0), 0, bar(DOFULL0), 0, W);
-    if (ok) {
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) {
-        issue_S(0);
-        issue_dP(0);
-      }
-      __syncwarp();
-    }
+    bool ok = warp_wait(bar(KV_FULL), 0, W);
     unsigned n_exec = 0, n_masked = 0;  // tile-pair accounting (pair_count)
-    for (int i = 0; ok && i < n_iter; ++i) {
-      const int st = i & 1;
-      const int sd = i % kDoSt;
-      const uint32_t ph = i & 1;
-      // dV += P^T dO   (A = P^T from TMEM: the 16-query k-steps 2g, 2g+1 in
-      // columns [32g, 32g + 16)); dO(i) is free once this has read it.  With
-      // two S buffers dV(i-1) is also confirmed here (before DV_DONE(i) is
-      // committed), freeing the buffer S(i+1) goes into.
-      ok = kSB == 2 && i > 0 ? warp_wait2(bar(P_FULL), ph, bar(DV_DONE), ph ^ 1, W) : warp_wait(bar(P_FULL), ph, W);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          ptx::mma_ts(tdV, tS(i) + (kk >> 1) * 32 + (kk & 1) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
-        ptx::tc_commit(bar(DV_DONE));
-        ptx::tc_commit(bar(DOEMPTY0 + sd));
+    if (warp == kMmaWarp) {
+      if (ok && (ok = warp_wait(bar(QFULL0), 0, W))) {
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) issue_S(0);
+        __syncwarp();
       }
-      __syncwarp();
-      // S^T(i+1) = K Q(i+1)^T once its buffer's last reader is done: dV(i)
-      // with one buffer, dV(i-1) (confirmed above) with two
-      if (i + 1 < n_iter) {
-        ok = kSB == 2 ? warp_wait(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W)
-                      : warp_wait2(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, bar(DV_DONE), ph, W);
+      for (int i = 0; ok && i < n_iter; ++i) {
+        const int st = i & 1;
+        const int sd = i % kDoSt;
+        const uint32_t ph = i & 1;
+        // dV += P^T dO   (A = P^T from TMEM: the 16-query k-steps 2g, 2g+1
+        // in columns [32g, 32g + 16)) once P(i) is there and dO(i) has landed
+        // (P(i) does not imply dO(i); the other MMA warp's dP(i) waits for it
+        // too).  With two S buffers dV(i-1) is also confirmed here (before
+        // DV_DONE(i) is committed), freeing the buffer S(i+1) goes into.
+        ok = warp_wait2(bar(P_FULL), ph, bar(DOFULL0 + sd), (i / kDoSt) & 1, W) &&
+             (kSB != 2 || i == 0 || warp_wait(bar(DV_DONE), ph ^ 1, W));
         if (!ok) break;
         ptx::tc_fence_after();
-        if (ptx::elect_one()) issue_S(i + 1);
+        if (ptx::elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            ptx::mma_ts(tdV, tS(i) + (kk >> 1) * 32 + (kk & 1) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
+          ptx::tc_commit(bar(DV_DONE));
+          ptx::tc_commit(bar(DOEMPTY0 + sd));
+        }
         __syncwarp();
+        // S^T(i+1) = K Q(i+1)^T once its buffer's last reader is done: dV(i)
+        // with one buffer, dV(i-1) (confirmed above) with two
+        if (i + 1 < n_iter) {
+          ok = kSB == 2 ? warp_wait(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W)
+                        : warp_wait2(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, bar(DV_DONE), ph, W);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) issue_S(i + 1);
+          __syncwarp();
+        }
       }
-      // dQ = dS K ;  dK += dS^T Q.  dQ first so the drain starts early.  The
-      // compute warps overwrite dS only after DP_FULL of the next block,
-      // which completes after this dK.
-      if (!(ok = warp_wait(bar(DS_FULL), ph, W))) break;
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk) ptx::mma_ss(tdQ, mndesc(sdS, kk), mndesc(sK, kk), kIdQ, kk > 0);
-        ptx::tc_commit(bar(DQ_FULL));
-#pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          ptx::mma_ss(tdK, kdesc(sdS, kk), mndesc(sQ(st), kk), kIdKV, (i | kk) != 0);
-        ptx::tc_commit(bar(QEMPTY0 + st));
-      }
-      __syncwarp();
-      if constexpr (kCount) {
-        ++n_exec;
-        n_masked += block_sees_key(q_first + i, k0, prm.N, prm.offset, prm.causal) ? 0u : 1u;
-      }
-      // dP(i+1) once dQ(i) has been drained and dO(i+1) has landed
-      if (i + 1 < n_iter) {
-        const int sd1 = (i + 1) % kDoSt;
-        if (!(ok = warp_wait2(bar(DQ_EMPTY), ph, bar(DOFULL0 + sd1), ((i + 1) / kDoSt) & 1, W))) break;
+    } else {
+      if (ok && (ok = warp_wait(bar(DOFULL0), 0, W))) {
         ptx::tc_fence_after();
-        if (ptx::elect_one()) issue_dP(sd1);
+        if (ptx::elect_one()) issue_dP(0);
         __syncwarp();
+      }
+      for (int i = 0; ok && i < n_iter; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = i & 1;
+        // dQ = dS K ;  dK += dS^T Q.  dQ first so the drain starts early.  The
+        // compute warps overwrite dS only after DP_FULL of the next block,
+        // which completes after this dK.  S(i) read Q(i) before P(i) existed,
+        // so dK(i) is its last reader.
+        if (!(ok = warp_wait(bar(DS_FULL), ph, W))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk) ptx::mma_ss(tdQ, mndesc(sdS, kk), mndesc(sK, kk), kIdQ, kk > 0);
+          ptx::tc_commit(bar(DQ_FULL));
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            ptx::mma_ss(tdK, kdesc(sdS, kk), mndesc(sQ(st), kk), kIdKV, (i | kk) != 0);
+          ptx::tc_commit(bar(QEMPTY0 + st));
+        }
+        __syncwarp();
+        if constexpr (kCount) {
+          ++n_exec;
+          n_masked += block_sees_key(q_first + i, k0, prm.N, prm.offset, prm.causal) ? 0u : 1u;
+        }
+        // dP(i+1) once dQ(i) has been drained and dO(i+1) has landed
+        if (i + 1 < n_iter) {
+          const int sd1 = (i + 1) % kDoSt;
+          if (!(ok = warp_wait2(bar(DQ_EMPTY), ph, bar(DOFULL0 + sd1), ((i + 1) / kDoSt) & 1, W))) break;
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) issue_dP(sd1);
+          __syncwarp();
+        }
       }
     }
     const bool lead = ptx::elect_one();
     if (lead) ptx::tc_commit(bar(ACC_FULL));
-    if (kCount && lead) {
+    if (kCount && lead && warp == kMma2Warp) {
       atomicAdd(prm.pair_count, (unsigned long long)n_exec);
       atomicAdd(prm.pair_count + 1, (unsigned long long)n_masked);
     }
     __syncwarp();
-    if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);  // nothing in flight at exit
+    // nothing in flight at exit (the other MMA warp commits too, on its way out)
+    if (!ok) ptx::wait_bounded(bar(ACC_FULL), 0, W, false);
   } else if (warp >= kDrainWarp0) {
     // ------------------------------------------------------------ dQ drain
     // One warp per TMEM lane quarter reads its 32 query rows of dQ(i) out of
