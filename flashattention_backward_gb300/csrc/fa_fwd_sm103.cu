@@ -28,8 +28,9 @@
 // Warp roles (352 threads):
 //   warps 0-7  softmax.  Warp w owns query rows 32*(w%4) .. +31 (its TMEM lane
 //              quarter) and the key columns of half w/4 of each block; the two
-//              warps of a lane quarter exchange row maxima through shared
-//              memory.  Epilogue: O columns [d/2 * (w/4), +d/2) and L.
+//              warps of a lane quarter exchange row maxima through a dead
+//              column of their S halves in tensor memory, and the final row
+//              sums through shared memory.  Epilogue: O columns [d/2 * (w/4), +d/2) and L.
 //   warp  8    TMA producer of Q (once) and K.
 //   warp  9    TMEM allocator and MMA issuer (one elected lane).
 //   warp 10    TMA producer of V.
@@ -94,8 +95,8 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQTile;                // kKSt tiles
   static constexpr int kV = kK + kKSt * kKVTile;        // kVStages tiles
-  static constexpr int kX = kV + kVStages * kKVTile;    // exchange: [2 parities (max) + 1 (sum)][2 halves][128] fp32
-  static constexpr int kBar = kX + 3 * 2 * kBlk * 4;
+  static constexpr int kX = kV + kVStages * kKVTile;    // row-sum exchange: [2 halves][128] fp32
+  static constexpr int kBar = kX + 2 * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr uint32_t kColO = LD == 256 ? 256 : kSBufs * BK;  // S/P buffers at 0, BK, 2 BK
@@ -317,7 +318,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_part = 0.f;                    // this warp's part of the row sum
     bool ok = true;
     for (int j = 0; j < n_blk; ++j) {
-      const int st = j & 1;            // parity of the row-maximum exchange slot
       const int sb = j % kSBufs;       // TMEM buffer of S_j / P_j
       const uint32_t tS = tm + sb * BK;
       if (!(ok = warp_wait(bar(S_FULL0 + sb), (j / kSBufs) & 1, W))) break;
@@ -342,10 +342,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < KC; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r[c]));
       float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-      // row maximum over both halves of the block
-      xchg[(st * 2 + G) * kBlk + t] = mx;
+      // row maximum over both halves of the block, exchanged through tensor
+      // memory (a shared-memory load would queue behind the score MMAs'
+      // operand reads): each warp parks its maximum in the last column of its
+      // own S half, which is dead once loaded and which P does not overwrite
+      ptx::tmem_st1(tS + lane_off + c0 + KC - 1, __float_as_uint(mx));
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();
       named_bar_sync(1 + qq, 64);
-      mx = fmaxf(mx, xchg[(st * 2 + (G ^ 1)) * kBlk + t]);
+      ptx::tc_fence_after();
+      mx = fmaxf(mx, __uint_as_float(ptx::tmem_ld1(tS + lane_off + (c0 ^ KC) + KC - 1)));
       float m_new = m_run;
       bool rescale = false;
       if (j == 0 || mx > m_run + kRescaleThreshold) {
@@ -388,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // epilogue: O / l and L
     if (ok) {
-      xchg[(4 + G) * kBlk + t] = l_part;
+      xchg[G * kBlk + t] = l_part;
       named_bar_sync(1 + qq, 64);
-      const float l = l_part + xchg[(4 + (G ^ 1)) * kBlk + t];
+      const float l = l_part + xchg[(G ^ 1) * kBlk + t];
       // A row that sees no key (l = 0; every row of a block with n_blk = 0,
       // whose O in tensor memory was never written) stores O = 0, L = +inf.
       if (n_blk == 0 || warp_wait(bar(O_DONE0 + (n_blk - 1) % kSBufs), ((n_blk - 1) / kSBufs) & 1, W)) {
