@@ -25,15 +25,16 @@
 // on those rare steps.  The final O / l and L = m + log l are exact for any
 // base.
 //
-// Warp roles (352 threads):
-//   warps 0-7  softmax.  Warp w owns query rows 32*(w%4) .. +31 (its TMEM lane
-//              quarter) and the key columns of half w/4 of each block; the two
-//              warps of a lane quarter exchange row maxima through a dead
-//              column of their S halves in tensor memory, and the final row
-//              sums through shared memory.  Epilogue: O columns [d/2 * (w/4), +d/2) and L.
-//   warp  8    TMA producer of Q (once) and K.
-//   warp  9    TMEM allocator and MMA issuer (one elected lane).
-//   warp 10    TMA producer of V.
+// Warp roles (608 threads; 352 at d = 256):
+//   warps 0-15 softmax (0-7 at d = 256).  Warp w owns query rows
+//              32*(w%4) .. +31 (its TMEM lane quarter) and 32 key columns of
+//              each block (column group w/4).  The warps of a lane quarter
+//              exchange row maxima through a dead column of their S slices in
+//              tensor memory, and the final row sums through shared memory.
+//              Epilogue (the first two warps of each lane quarter): O columns
+//              [d/2 * (w/4), +d/2) and L.
+//   then       TMA producer of Q (once) and K; TMEM allocator and MMA issuer
+//              (one elected lane); TMA producer of V.
 //
 // Every wait is bounded (same mechanism as the backward kernel).
 
@@ -53,8 +54,6 @@ namespace fa {
 namespace {
 
 constexpr int kBlk = 128;
-constexpr int kThreads = 352;
-constexpr int kSoftmaxThreads = 256;
 constexpr int kKStages = 3;  // K tiles in shared memory (at most; two at d = 256)
 constexpr int kVStages = 2;  // V tiles in shared memory
 constexpr int kSBufs = 3;    // S/P buffers in TMEM
@@ -86,6 +85,15 @@ enum BarId {
 // past d.  Key blocks are BK rows: 128, or 64 at LD = 256.
 template <int LD>
 struct FwdLayout {
+  // softmax warps: four per TMEM lane quarter, each on 32 key columns of a
+  // block (two at d = 256, whose blocks have 64 keys)
+  static constexpr int kGroups = LD == 256 ? 2 : 4;     // softmax warps per lane quarter
+  static constexpr int kSmWarps = 4 * kGroups;
+  static constexpr int kSmThreads = 32 * kSmWarps;
+  static constexpr int kProdK = kSmWarps;               // TMA producer of Q and K
+  static constexpr int kMma = kSmWarps + 1;             // TMEM allocator, MMA issuer
+  static constexpr int kProdV = kSmWarps + 2;           // TMA producer of V
+  static constexpr int kThreads = 32 * (kSmWarps + 3);
   static constexpr int BK = LD == 256 ? 64 : 128;       // keys per block
   static constexpr int kKSt = LD == 256 ? 2 : kKStages;  // K stages
   static constexpr int kQChunk = kBlk * 128;            // 128 rows x 64 columns
@@ -95,8 +103,8 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQTile;                // kKSt tiles
   static constexpr int kV = kK + kKSt * kKVTile;        // kVStages tiles
-  static constexpr int kX = kV + kVStages * kKVTile;    // row-sum exchange: [2 halves][128] fp32
-  static constexpr int kBar = kX + 2 * kBlk * 4;
+  static constexpr int kX = kV + kVStages * kKVTile;    // row-sum exchange: [kGroups][128] fp32
+  static constexpr int kBar = kX + kGroups * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr uint32_t kColO = LD == 256 ? 256 : kSBufs * BK;  // S/P buffers at 0, BK, 2 BK
@@ -125,14 +133,17 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+constexpr int fwd_ld(int hd) { return hd <= 64 ? 64 : (hd <= 128 ? 128 : 256); }
+
 template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const FwdParams prm) {
-  constexpr int LD = HD <= 64 ? 64 : (HD <= 128 ? 128 : 256);
+  constexpr int LD = fwd_ld(HD);
   using Ly = FwdLayout<LD>;
   constexpr int BK = Ly::BK;       // keys per block
-  constexpr int KC = BK / 2;       // key columns per softmax warp
+  constexpr int NG = Ly::kGroups;  // softmax warps per lane quarter
+  constexpr int KC = BK / NG;      // key columns per softmax warp (32)
   constexpr int kKSt = Ly::kKSt;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = ptx::smem_addr(smem);
@@ -147,13 +158,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      ptx::mbar_init(bar(i), (i >= P_FULL0 && i < P_FULL0 + kSBufs)     ? kSoftmaxThreads + 1
+      ptx::mbar_init(bar(i), (i >= P_FULL0 && i < P_FULL0 + kSBufs)     ? Ly::kSmThreads + 1
                              : (i >= S_READY0 && i < S_READY0 + kSBufs) ? 2
                                                                         : 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == Ly::kMma) {
     ptx::tmem_alloc(sbase + Ly::kMisc, Ly::kTmemCols);
     ptx::tmem_relinquish();
     ptx::tc_fence_before();
@@ -188,15 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sK = [&](int st) -> uint32_t { return sbase + Ly::kK + st * Ly::kKVTile; };
   auto sV = [&](int st) -> uint32_t { return sbase + Ly::kV + st * Ly::kKVTile; };
 
-  if (warp == 8 || warp == 10) {
+  if (warp == Ly::kProdK || warp == Ly::kProdV) {
     // ------------------------------------------------------------ producers
-    // warp 8: Q once, then K_b into stage b % kKSt once S_{b-kKSt} has read it;
-    // warp 10: V_b into stage b % 2 once O += P_{b-2} V_{b-2} has read it.
+    // K producer: Q once, then K_b into stage b % kKSt once S_{b-kKSt} has
+    // read it; V producer: V_b into stage b % 2 once O += P_{b-2} V_{b-2} has
+    // read it.
     // Each producer waits for its own copies and forwards their completion
     // (K_b to S_READY, V_b to P_FULL), so the MMA warp waits on two
     // barriers per block.  Forwarding block b-1 after issuing block b keeps
     // one copy in flight while the previous one is confirmed.
-    const bool isK = warp == 8;
+    const bool isK = warp == Ly::kProdK;
     const int nst = isK ? kKSt : kVStages;
     const int full0 = isK ? K_FULL0 : V_FULL0, empty0 = isK ? K_EMPTY0 : V_EMPTY0;
     const CUtensorMap* map = isK ? &tmK : &tmV;
@@ -249,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (isK && n_blk > 0) ptx::wait_bounded(bar(Q_FULL), 0, W, false);
       for (int j = forwarded; j < issued; ++j) ptx::wait_bounded(bar(full0 + j % nst), (j / nst) & 1, W, false);
     }
-  } else if (warp == 9) {
+  } else if (warp == Ly::kMma) {
     // ------------------------------------------------------------ MMA issue
     // order: S_0, S_1, then per block b: S_{b+2}, O += P_b V_b
     constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, BK, false, false);  // S = Q K^T
@@ -285,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_{j+2} first: it only waits for O += P_{j-1} V_{j-1}, so the score
       // block two ahead is in flight while the softmax warps finish P_j
       if (j + 2 < n_blk && !(ok = issue_S(j + 2))) break;
-      // O += P_j V_j  (A = P_j from TMEM: the 16-key steps of softmax half g in
-      // columns [g KC, g KC + KC/2))
+      // O += P_j V_j  (A = P_j from TMEM: the 16-key steps of softmax warp g
+      // of a lane quarter in columns [g KC, g KC + KC/2))
       if (!(ok = warp_wait(bar(P_FULL0 + sb), (j / kSBufs) & 1, W))) break;  // P_j and V_j
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
@@ -342,16 +354,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < KC; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(r[c]));
       float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
-      // row maximum over both halves of the block, exchanged through tensor
+      // row maximum over the lane quarter's warps, exchanged through tensor
       // memory (a shared-memory load would queue behind the score MMAs'
       // operand reads): each warp parks its maximum in the last column of its
-      // own S half, which is dead once loaded and which P does not overwrite
+      // own S slice, which is dead once loaded and which P does not overwrite
       ptx::tmem_st1(tS + lane_off + c0 + KC - 1, __float_as_uint(mx));
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      named_bar_sync(1 + qq, 64);
+      named_bar_sync(1 + qq, 32 * NG);
       ptx::tc_fence_after();
-      mx = fmaxf(mx, __uint_as_float(ptx::tmem_ld1(tS + lane_off + (c0 ^ KC) + KC - 1)));
+      if constexpr (NG == 2) {
+        mx = fmaxf(mx, __uint_as_float(ptx::tmem_ld1(tS + lane_off + (c0 ^ KC) + KC - 1)));
+      } else {
+        uint32_t o3[3];
+        ptx::tmem_ld1x3(tS + lane_off + ((G + 1) % NG) * KC + KC - 1, tS + lane_off + ((G + 2) % NG) * KC + KC - 1,
+                        tS + lane_off + ((G + 3) % NG) * KC + KC - 1, o3);
+        mx = fmaxf(fmaxf(mx, __uint_as_float(o3[0])), fmaxf(__uint_as_float(o3[1]), __uint_as_float(o3[2])));
+      }
       float m_new = m_run;
       bool rescale = false;
       if (j == 0 || mx > m_run + kRescaleThreshold) {
@@ -359,21 +378,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = j > 0;
       }
       if (__any_sync(0xffffffffu, rescale)) {
-        // O (this warp's columns) and l move to the new base: O *= 2^(m - m')
-        if (!(ok = warp_wait(bar(O_DONE0 + (j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, W))) break;
-        ptx::tc_fence_after();
+        // O and l move to the new base: O *= 2^(m - m').  O's columns belong
+        // to the first two warps of the lane quarter, half each.
         const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.f;
-        constexpr int kOC = HD / 2;  // this warp's O columns, in 16-column pieces
-#pragma unroll
-        for (int c = 0; c < kOC; c += 16) {
-          uint32_t o[16];
-          ptx::tmem_ld16(tm + Ly::kColO + lane_off + G * kOC + c, o);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          ptx::tmem_st16(tm + Ly::kColO + lane_off + G * kOC + c, o);
-        }
-        ptx::tmem_st_wait();
         l_part *= alpha;
+        if (G < 2) {
+          if (!(ok = warp_wait(bar(O_DONE0 + (j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, W))) break;
+          ptx::tc_fence_after();
+          constexpr int kOC = HD / 2;  // this warp's O columns, in 16-column pieces
+#pragma unroll
+          for (int c = 0; c < kOC; c += 16) {
+            uint32_t o[16];
+            ptx::tmem_ld16(tm + Ly::kColO + lane_off + G * kOC + c, o);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st16(tm + Ly::kColO + lane_off + G * kOC + c, o);
+          }
+          ptx::tmem_st_wait();
+        }
       }
       m_run = m_new;
       const float mb = m_run == -INFINITY ? 0.f : m_run;
@@ -395,11 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: O / l and L
     if (ok) {
       xchg[G * kBlk + t] = l_part;
-      named_bar_sync(1 + qq, 64);
-      const float l = l_part + xchg[(G ^ 1) * kBlk + t];
+      named_bar_sync(1 + qq, 32 * NG);
+      float l = 0.f;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) l += xchg[g * kBlk + t];
       // A row that sees no key (l = 0; every row of a block with n_blk = 0,
       // whose O in tensor memory was never written) stores O = 0, L = +inf.
-      if (n_blk == 0 || warp_wait(bar(O_DONE0 + (n_blk - 1) % kSBufs), ((n_blk - 1) / kSBufs) & 1, W)) {
+      // O's columns and L belong to the first two warps of the lane quarter
+      if (G < 2 && (n_blk == 0 || warp_wait(bar(O_DONE0 + (n_blk - 1) % kSBufs), ((n_blk - 1) / kSBufs) & 1, W))) {
         ptx::tc_fence_after();
         const bool empty = !(l > 0.f);
         const float inv = empty ? 0.f : 1.f / l;
@@ -438,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == Ly::kMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tm, Ly::kTmemCols);
   }
@@ -446,11 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int HD>
 cudaError_t launch_fwd_hd(const fa_problem& p, const CUtensorMap* maps, const FwdParams& prm, cudaStream_t s) {
-  using Ly = FwdLayout<(HD <= 64 ? 64 : (HD <= 128 ? 128 : 256))>;
+  using Ly = FwdLayout<fwd_ld(HD)>;
   cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
-  fwd_sm103_kernel<HD><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], prm);
+  fwd_sm103_kernel<HD><<<grid, Ly::kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], prm);
   return cudaGetLastError();
 }
 

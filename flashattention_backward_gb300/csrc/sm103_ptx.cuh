@@ -240,6 +240,17 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
+// Three single columns, one wait.
+__device__ __forceinline__ void tmem_ld1x3(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t (&r)[3]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%3];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%1}, [%4];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%2}, [%5];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2])
+      : "r"(a0), "r"(a1), "r"(a2)
+      : "memory");
+}
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
   uint32_t r;
   asm volatile(
