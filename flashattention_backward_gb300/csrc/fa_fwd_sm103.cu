@@ -10,9 +10,9 @@
 // the key blocks it can see (all, or up to the diagonal under the causal
 // mask).  S_b = Q K_b^T goes to one of three TMEM buffers; P_b (bf16) is
 // written over S_b and feeds O += P_b V_b straight from TMEM; O accumulates
-// in TMEM.  With three buffers S_{b+2} is issued as soon as O += P_{b-1} V_{b-1}
-// has read its buffer, ahead of O += P_b V_b, so the tensor pipe computes the
-// score block two ahead while the softmax warps still work on P_b.
+// in TMEM.  With three buffers S_b can be computed while the softmax warps
+// still work on P_{b-1} and P_{b-2}; S_b and O += P_b V_b are issued by two
+// warps, each waiting only for its own inputs.
 // K lives in three shared-memory stages (two at d = 256), each freed as soon
 // as its S block is done; V in two, each freed when its O += P V is done.
 // At d = 256 the 64-key blocks keep a 64 KB Q tile and two stages each of K
@@ -25,7 +25,7 @@
 // on those rare steps.  The final O / l and L = m + log l are exact for any
 // base.
 //
-// Warp roles (608 threads; 352 at d = 256):
+// Warp roles (640 threads; 352 at d = 256):
 //   warps 0-15 softmax (0-7 at d = 256).  Warp w owns query rows
 //              32*(w%4) .. +31 (its TMEM lane quarter) and 32 key columns of
 //              each block (column group w/4).  The warps of a lane quarter
@@ -33,8 +33,10 @@
 //              tensor memory, and the final row sums through shared memory.
 //              Epilogue (the first two warps of each lane quarter): O columns
 //              [d/2 * (w/4), +d/2) and L.
-//   then       TMA producer of Q (once) and K; TMEM allocator and MMA issuer
-//              (one elected lane); TMA producer of V.
+//   then       TMA producer of Q (once) and K; TMEM allocator and issuer of
+//              the S products; TMA producer of V; issuer of O += P V (one
+//              elected lane in each MMA warp; at d = 256 the allocator's warp
+//              issues both).
 //
 // Every wait is bounded (same mechanism as the backward kernel).
 
@@ -74,9 +76,11 @@ enum BarId {
   P_FULL0 = S_FULL0 + kSBufs,      // P_b in buffer b % 3 and V_b forwarded (256 + 1 arrivals)
   O_DONE0 = P_FULL0 + kSBufs,      // O += P_b V_b (and every MMA before it) done, on
                                    // barrier b % 3.  The softmax warps ask about block b-1
-                                   // only after S_b, whose commit proves O += P_{b-3} V_{b-3}
+                                   // only after S_b, which is issued only once O += P_{b-3}
+                                   // V_{b-3} (and every earlier product of that chain) is
                                    // done, so the parity always names the current phase
-  DRAIN = O_DONE0 + kSBufs,        // every MMA done (waited only when a CTA gives up)
+  DRAIN = O_DONE0 + kSBufs,        // every MMA of both MMA warps done (waited only when a
+                                   // CTA gives up)
   kNumBars
 };
 
@@ -90,10 +94,14 @@ struct FwdLayout {
   static constexpr int kGroups = LD == 256 ? 2 : 4;     // softmax warps per lane quarter
   static constexpr int kSmWarps = 4 * kGroups;
   static constexpr int kSmThreads = 32 * kSmWarps;
+  // MMA issue split over two warps (S products; O += P V products) at
+  // d <= 128; at d = 256 the split measured 13 % slower and one warp issues both
+  static constexpr bool kSplitMma = LD != 256;
   static constexpr int kProdK = kSmWarps;               // TMA producer of Q and K
-  static constexpr int kMma = kSmWarps + 1;             // TMEM allocator, MMA issuer
+  static constexpr int kMma = kSmWarps + 1;             // TMEM allocator; issues the S products
   static constexpr int kProdV = kSmWarps + 2;           // TMA producer of V
-  static constexpr int kThreads = 32 * (kSmWarps + 3);
+  static constexpr int kMmaPV = kSplitMma ? kSmWarps + 3 : kMma;  // issues the O += P V products
+  static constexpr int kThreads = 32 * (kSmWarps + (kSplitMma ? 4 : 3));
   static constexpr int BK = LD == 256 ? 64 : 128;       // keys per block
   static constexpr int kKSt = LD == 256 ? 2 : kKStages;  // K stages
   static constexpr int kQChunk = kBlk * 128;            // 128 rows x 64 columns
@@ -160,6 +168,7 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
     for (int i = 0; i < kNumBars; ++i)
       ptx::mbar_init(bar(i), (i >= P_FULL0 && i < P_FULL0 + kSBufs)     ? Ly::kSmThreads + 1
                              : (i >= S_READY0 && i < S_READY0 + kSBufs) ? 2
+                             : i == DRAIN                               ? (Ly::kSplitMma ? 2 : 1)
                                                                         : 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -261,9 +270,14 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
       if (isK && n_blk > 0) ptx::wait_bounded(bar(Q_FULL), 0, W, false);
       for (int j = forwarded; j < issued; ++j) ptx::wait_bounded(bar(full0 + j % nst), (j / nst) & 1, W, false);
     }
-  } else if (warp == Ly::kMma) {
+  } else if (warp == Ly::kMma || warp == Ly::kMmaPV) {
     // ------------------------------------------------------------ MMA issue
-    // order: S_0, S_1, then per block b: S_{b+2}, O += P_b V_b
+    // At d <= 128 two warps run two independent chains: one issues S_j as
+    // soon as K_j has landed and O += P_{j-3} V_{j-3} has read its buffer; the
+    // other issues O += P_j V_j as soon as P_j is in its buffer and V_j has
+    // landed.  With one warp issuing both, S_{j+2} waited behind the wait for
+    // P_j (or, issued first, for O += P_{j-1} V_{j-1} to complete), and the
+    // softmax warps waited for their S block every block (clock64 stamps).
     constexpr uint32_t kIdS = ptx::idesc_bf16_f32(128, BK, false, false);  // S = Q K^T
     constexpr uint32_t kIdO = ptx::idesc_bf16_f32(128, HD, false, true);   // O += P V
     auto kdesc = [&](uint32_t tile, uint32_t chunk, int kk) -> uint64_t {
@@ -290,16 +304,11 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
       __syncwarp();
       return true;
     };
-    bool ok = n_blk == 0 || (warp_wait(bar(Q_FULL), 0, W) && issue_S(0));
-    if (ok && n_blk > 1) ok = issue_S(1);
-    for (int j = 0; ok && j < n_blk; ++j) {
+    // O += P_j V_j  (A = P_j from TMEM: the 16-key steps of softmax warp g
+    // of a lane quarter in columns [g KC, g KC + KC/2)) once P_j and V_j are there
+    auto issue_PV = [&](int j) -> bool {
       const int sb = j % kSBufs, vs = j % kVStages;
-      // S_{j+2} first: it only waits for O += P_{j-1} V_{j-1}, so the score
-      // block two ahead is in flight while the softmax warps finish P_j
-      if (j + 2 < n_blk && !(ok = issue_S(j + 2))) break;
-      // O += P_j V_j  (A = P_j from TMEM: the 16-key steps of softmax warp g
-      // of a lane quarter in columns [g KC, g KC + KC/2))
-      if (!(ok = warp_wait(bar(P_FULL0 + sb), (j / kSBufs) & 1, W))) break;  // P_j and V_j
+      if (!warp_wait(bar(P_FULL0 + sb), (j / kSBufs) & 1, W)) return false;  // P_j and V_j
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
         const uint32_t tP = tm + sb * BK;
@@ -311,6 +320,21 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
         ptx::tc_commit(bar(V_EMPTY0 + vs));
       }
       __syncwarp();
+      return true;
+    };
+    bool ok = n_blk == 0 || (Ly::kSplitMma && warp == Ly::kMmaPV) || warp_wait(bar(Q_FULL), 0, W);
+    if constexpr (Ly::kSplitMma) {
+      if (warp == Ly::kMma)
+        for (int j = 0; ok && j < n_blk; ++j) ok = issue_S(j);
+      else
+        for (int j = 0; ok && j < n_blk; ++j) ok = issue_PV(j);
+    } else {
+      // one warp: S_0, S_1, then per block S_{j+2} first (it waits only for
+      // O += P_{j-1} V_{j-1}, so the score block two ahead is in flight while
+      // the softmax warps finish P_j) and O += P_j V_j
+      if (ok && n_blk > 0) ok = issue_S(0);
+      if (ok && n_blk > 1) ok = issue_S(1);
+      for (int j = 0; ok && j < n_blk; ++j) ok = (j + 2 >= n_blk || issue_S(j + 2)) && issue_PV(j);
     }
     // the softmax warps wait for the last O_DONE; on an abort make sure no
     // MMA is still in flight before tensor memory is freed
