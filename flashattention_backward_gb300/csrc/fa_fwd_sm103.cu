@@ -73,7 +73,7 @@ enum BarId {
   S_READY0 = V_EMPTY0 + kVStages,  // S_b may be issued: K_b forwarded by its producer and
                                    // buffer b % 3 read by O += P_{b-3} V_{b-3} (2 arrivals)
   S_FULL0 = S_READY0 + kSBufs,     // S_b in TMEM buffer b % 3
-  P_FULL0 = S_FULL0 + kSBufs,      // P_b in buffer b % 3 and V_b forwarded (256 + 1 arrivals)
+  P_FULL0 = S_FULL0 + kSBufs,      // P_b in buffer b % 3 and V_b forwarded (softmax threads + 1)
   O_DONE0 = P_FULL0 + kSBufs,      // O += P_b V_b (and every MMA before it) done, on
                                    // barrier b % 3.  The softmax warps ask about block b-1
                                    // only after S_b, which is issued only once O += P_{b-3}
