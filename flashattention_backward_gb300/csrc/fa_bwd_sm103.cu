@@ -35,17 +35,23 @@
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128)     S^T; P^T (bf16) is written over it: query columns
 //               [32g, 32g + 32) of S become P columns [32g, 32g + 16)
-//   [128,256)   dP^T, then the dQ tile of the same step written over it
+//   [128,256)   dP^T (d > 64: then the dQ tile of the same step over it)
 //   [256,256+d) dV accumulator, [256+LD,256+LD+d) dK accumulator (LD = 64
 //               for d <= 64, else 128)
+//   [384,512)   d <= 64: a second S^T/P^T buffer for odd query blocks; dQ(i)
+//               goes into the first d columns of S buffer i % 2 once dV(i)
+//               has read P(i) there
 //
 // MMA issue order per query block i (software pipelined), per MMA warp:
 //   warp 21:  dV(i)  S(i+1)
-//   warp 22:  dQ(i)  dK(i)  dP(i+1)
-// dQ goes first so that its drain starts early, and dP(i+1) is issued as soon
-// as the drain warps have read dQ(i) out of the columns dP shares, so the
-// tensor pipe computes dP(i+1) while the compute warps turn S(i+1) into
-// P(i+1).
+//   warp 22:  d > 64:   dQ(i)  dK(i)  dP(i+1)
+//             d <= 64:  dP(i+1)  dQ(i)  dK(i)
+// dQ goes before dK so that its drain starts early.  For d > 64, dP(i+1) is
+// issued as soon as the drain warps have read dQ(i) out of the columns dP
+// shares, so the tensor pipe computes dP(i+1) while the compute warps turn
+// S(i+1) into P(i+1).  For d <= 64 (smaller products, so the hand-offs weigh
+// more) dP(i+1) only waits until the compute warps have read dP(i) into
+// registers, and dS is double-buffered in shared memory.
 //
 // Every wait is bounded; when one runs out the CTA records FA_ERR_TIMEOUT,
 // drains its own TMA loads, MMAs and bulk reductions, frees tensor memory and
@@ -82,6 +88,8 @@ constexpr int kStagedUnits = 4;                 // dQ units per drain warp stage
 constexpr int kHeadGroup = 4;  // heads whose key blocks interleave in the single-launch grid order
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Barriers a block of head dim > 64 uses come first; the third Q and dO
+// stages and the second S buffer's barriers of head dims <= 64 follow.
 enum BarId {
   KV_FULL = 0,  // K, V landed
   QFULL0,       // Q stage (with its L, D rows) landed; 32 arrivals
@@ -90,48 +98,87 @@ enum BarId {
   QEMPTY1,
   DOFULL0,      // dO stage landed
   DOFULL1,
-  DOEMPTY0,     // dO stage free again
+  DOEMPTY0,     // dO stage free again (dV and dP commit)
   DOEMPTY1,
   S_FULL0,      // S^T(i) in TMEM buffer i % kSBufs (one barrier per buffer)
   S_FULL1,
   P_FULL,       // P^T(i) in TMEM (one per compute thread)
-  DV_DONE,      // dV(i) product done: S/P columns reusable
+  DV_DONE0,     // dV(i) product done: P(i) read out of S buffer i % kSBufs
   DP_FULL,      // dP^T(i) in TMEM
   DS_FULL,      // dS^T(i) in shared memory (one per compute thread)
-  DQ_FULL,      // dQ(i) in TMEM
-  DQ_EMPTY,     // dQ(i) drained from TMEM (one per drain thread)
+  DQ_FULL0,     // dQ(i) in TMEM (two S buffers: one barrier per buffer)
+  DQ_EMPTY0,    // dQ(i) drained from TMEM (one per drain thread)
   ACC_FULL,     // every MMA done: dK, dV final
+  QFULL2,
+  QEMPTY2,
+  DOFULL2,
+  DOEMPTY2,
+  S_READ0,      // two S buffers: S^T(i) read out of buffer i % 2 (one per compute thread)
+  S_READ1,
+  DV_DONE1,
+  DP_READ,      // two S buffers: dP^T(i) read out of TMEM (one per compute thread)
+  DS_EMPTY,     // two S buffers: dS(i) read by dK(i) and dQ(i)
+  DQ_FULL1,
+  DQ_EMPTY1,
   kNumBars
 };
+
+// Member s of the barrier set whose first member is `first` (stages, buffers).
+__device__ __forceinline__ int bar_member(int first, int s) {
+  switch (first) {
+    case QFULL0: return s == 0 ? QFULL0 : s == 1 ? QFULL1 : QFULL2;
+    case QEMPTY0: return s == 0 ? QEMPTY0 : s == 1 ? QEMPTY1 : QEMPTY2;
+    case DOFULL0: return s == 0 ? DOFULL0 : s == 1 ? DOFULL1 : DOFULL2;
+    case DOEMPTY0: return s == 0 ? DOEMPTY0 : s == 1 ? DOEMPTY1 : DOEMPTY2;
+    case DV_DONE0: return s == 0 ? DV_DONE0 : DV_DONE1;
+    case DQ_FULL0: return s == 0 ? DQ_FULL0 : DQ_FULL1;
+    case DQ_EMPTY0: return s == 0 ? DQ_EMPTY0 : DQ_EMPTY1;
+    default: return first + s;  // S_FULL0, S_READ0: consecutive
+  }
+}
+
+// Stage and phase parity of item i (>= 0) of a ring of N stages, in unsigned
+// arithmetic (a signed % or / costs several instructions in the per-block
+// loops, and the compute warps are issue-bound).
+template <int N>
+__device__ __forceinline__ int ring_stage(int i) { return (int)((unsigned)i % (unsigned)N); }
+template <int N>
+__device__ __forceinline__ uint32_t ring_phase(int i) { return ((unsigned)i / (unsigned)N) & 1u; }
 
 // Shared-memory and TMEM layout for tiles LD = 64 or 128 columns wide (head
 // dims 32 and 64 use LD = 64, 96 and 128 use LD = 128; the TMA zero-fills the
 // columns past d).
 template <int LD>
 struct Layout {
-  static constexpr int kDoStages = LD == 128 ? 1 : 2;
+  // Two S^T buffers where the accumulators leave room (LD = 64).  Then S(i+1)
+  // need not wait for dV(i) to read P(i); P(i) is packed into the lower 64
+  // columns of its buffer, and dQ(i) goes into the upper 64 columns of the
+  // other buffer once S(i+1) has been read out of it, so dP^T keeps its
+  // columns to itself.  Q and dO get three stages each, so that no TMA load
+  // sits inside the per-block chain of hand-offs.
+  static constexpr int kSBufs = LD == 64 ? 2 : 1;
+  static constexpr int kQStages = LD == 64 ? 3 : 2;
+  static constexpr int kDoStages = LD == 64 ? 3 : 1;
   static constexpr int kChunk = kBlk * 128;     // 128 rows x 128 bytes (64 bf16 columns)
   static constexpr int kTile = kBlk * LD * 2;   // one Q / K / V / dO tile
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
-  static constexpr int kQ = kV + kTile;                 // 2 stages
-  static constexpr int kdO = kQ + 2 * kTile;            // kDoStages stages
-  static constexpr int kdS = kdO + kDoStages * kTile;   // 128 x 128 bf16, two 64-column chunks
+  static constexpr int kQ = kV + kTile;                  // kQStages stages
+  static constexpr int kdO = kQ + kQStages * kTile;      // kDoStages stages
+  static constexpr int kdS = kdO + kDoStages * kTile;    // 128 x 128 bf16, two 64-column chunks
   // dQ staging for bulk reductions: one slot of kStagedUnits 2 KB units
   // (32 rows x 16 fp32 columns each) per drain warp
   static constexpr int kStage = kdS + 2 * kChunk;
   static constexpr int kStageBytes = kDrainWarps * kStagedUnits * 2048;
-  static constexpr int kL = kStage + kStageBytes;      // 2 stages x 128 fp32 (L * log2 e)
-  static constexpr int kD = kL + 2 * kBlk * 4;          // 2 stages x 128 fp32
-  static constexpr int kBar = kD + 2 * kBlk * 4;
-  static constexpr int kMisc = kBar + kNumBars * 8;     // TMEM base address, abort flag
+  static constexpr int kL = kStage + kStageBytes;        // kQStages x 128 fp32 (L * log2 e)
+  static constexpr int kD = kL + kQStages * kBlk * 4;    // kQStages x 128 fp32
+  static constexpr int kBar = kD + kQStages * kBlk * 4;
+  static constexpr int kMisc = kBar + kNumBars * 8;      // TMEM base address, abort flag
   static constexpr int kBytes = kMisc + 16;
-  // S^T buffers: two where the accumulators leave room (LD = 64), so that
-  // S(i+1) need not wait for dV(i) to read P(i)
-  static constexpr int kSBufs = LD == 64 ? 2 : 1;
   static constexpr uint32_t kColS = 0, kColS1 = 384, kColdP = 128, kColdQ = 128;
   static constexpr uint32_t kColdV = 256, kColdK = 256 + LD;
   static constexpr uint32_t kTmemCols = 512;
+  static_assert(kQStages <= 3 && kDoStages <= 3, "barrier slots");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -238,25 +285,30 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::kMisc + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + Ly::kBar + 8 * i; };
+  auto barm = [&](int first, int s) -> uint32_t { return bar(bar_member(first, s)); };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(KV_FULL), 1);
-    ptx::mbar_init(bar(QFULL0), 32);
-    ptx::mbar_init(bar(QFULL1), 32);
-    ptx::mbar_init(bar(QEMPTY0), 1);
-    ptx::mbar_init(bar(QEMPTY1), 1);
-    ptx::mbar_init(bar(DOFULL0), 1);
-    ptx::mbar_init(bar(DOFULL1), 1);
-    ptx::mbar_init(bar(DOEMPTY0), 2);  // dP (second MMA warp) and dV (first) read the stage
-    ptx::mbar_init(bar(DOEMPTY1), 2);
-    ptx::mbar_init(bar(S_FULL0), 1);
-    ptx::mbar_init(bar(S_FULL1), 1);
+    for (int st = 0; st < Ly::kQStages; ++st) {
+      ptx::mbar_init(barm(QFULL0, st), 32);
+      ptx::mbar_init(barm(QEMPTY0, st), 1);
+    }
+    for (int st = 0; st < kDoSt; ++st) {
+      ptx::mbar_init(barm(DOFULL0, st), 1);
+      ptx::mbar_init(barm(DOEMPTY0, st), 2);  // dP (second MMA warp) and dV (first) read the stage
+    }
+    for (int sb = 0; sb < 2; ++sb) {
+      ptx::mbar_init(barm(S_FULL0, sb), 1);
+      ptx::mbar_init(barm(S_READ0, sb), kComputeThreads);
+      ptx::mbar_init(barm(DV_DONE0, sb), 1);
+      ptx::mbar_init(barm(DQ_FULL0, sb), 1);
+      ptx::mbar_init(barm(DQ_EMPTY0, sb), kDrainThreads);
+    }
     ptx::mbar_init(bar(P_FULL), kComputeThreads);
-    ptx::mbar_init(bar(DV_DONE), 1);
     ptx::mbar_init(bar(DP_FULL), 1);
+    ptx::mbar_init(bar(DP_READ), kComputeThreads);
     ptx::mbar_init(bar(DS_FULL), kComputeThreads);
-    ptx::mbar_init(bar(DQ_FULL), 1);
-    ptx::mbar_init(bar(DQ_EMPTY), kDrainThreads);
+    ptx::mbar_init(bar(DS_EMPTY), 1);
     ptx::mbar_init(bar(ACC_FULL), 2);  // one commit from each MMA warp
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -295,7 +347,15 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
   const int64_t khead = (int64_t)b * prm.ksb + (int64_t)h * prm.ksh;
   const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
 
-  const uint32_t sK = sbase + Ly::kK, sV = sbase + Ly::kV, sdS = sbase + Ly::kdS;
+  const uint32_t sK = sbase + Ly::kK, sV = sbase + Ly::kV;
+  constexpr int kSB = Ly::kSBufs;
+  constexpr int kQSt = Ly::kQStages;
+  const uint32_t sdS = sbase + Ly::kdS;
+  // S^T buffer of query block i
+  auto tS = [&](int i) -> uint32_t { return tm + (kSB == 2 && (i & 1) ? Ly::kColS1 : Ly::kColS); };
+  // dQ(i): over dP^T with one S buffer; with two, the upper 64 columns of the
+  // buffer that S(i+1) uses (after S(i+1) has been read out of it)
+  auto tdQ = [&](int i) -> uint32_t { return kSB == 2 ? tS(i + 1) + 64 : tm + Ly::kColdQ; };
   auto sQ = [&](int st) -> uint32_t { return sbase + Ly::kQ + st * Ly::kTile; };
   auto sdO = [&](int st) -> uint32_t { return sbase + Ly::kdO + st * Ly::kTile; };
 
@@ -331,10 +391,10 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     };
     fetch_rows(0);
     for (int i = 0; i < n_iter; ++i) {
-      const int st = i & 1;
+      const int st = ring_stage<kQSt>(i);
       const int q0 = (q_first + i) * kBlk;
-      if (i >= 2) {
-        ok = warp_wait(bar(QEMPTY0 + st), ((i - 2) >> 1) & 1, W);
+      if (i >= kQSt) {
+        ok = warp_wait(barm(QEMPTY0, st), ring_phase<kQSt>(i - kQSt), W);
         if (!ok) break;
       }
       float* sL = reinterpret_cast<float*>(smem + Ly::kL) + st * kBlk;
@@ -346,24 +406,24 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       }
       __syncwarp();
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(QFULL0 + st), Ly::kTile);
+        ptx::mbar_arrive_expect_tx(barm(QFULL0, st), Ly::kTile);
 #pragma unroll
         for (int c = 0; c < LD / 64; ++c)
-          ptx::tma_load_4d(sQ(st) + c * Ly::kChunk, &tmQ, bar(QFULL0 + st), c * 64, q0, h, b);
+          ptx::tma_load_4d(sQ(st) + c * Ly::kChunk, &tmQ, barm(QFULL0, st), c * 64, q0, h, b);
       } else {
-        ptx::mbar_arrive(bar(QFULL0 + st));
+        ptx::mbar_arrive(barm(QFULL0, st));
       }
       q_issued = i + 1;
-      const int sd = i % kDoSt;
+      const int sd = ring_stage<kDoSt>(i);
       if (i >= kDoSt) {
-        ok = warp_wait(bar(DOEMPTY0 + sd), ((i - kDoSt) / kDoSt) & 1, W);
+        ok = warp_wait(barm(DOEMPTY0, sd), ring_phase<kDoSt>(i - kDoSt), W);
         if (!ok) break;
       }
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(bar(DOFULL0 + sd), Ly::kTile);
+        ptx::mbar_arrive_expect_tx(barm(DOFULL0, sd), Ly::kTile);
 #pragma unroll
         for (int c = 0; c < LD / 64; ++c)
-          ptx::tma_load_4d(sdO(sd) + c * Ly::kChunk, &tmdO, bar(DOFULL0 + sd), c * 64, q0, h, b);
+          ptx::tma_load_4d(sdO(sd) + c * Ly::kChunk, &tmdO, barm(DOFULL0, sd), c * 64, q0, h, b);
       }
       __syncwarp();
       do_issued = i + 1;
@@ -371,10 +431,10 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     }
     if (!ok) {  // let every copy this CTA started land before the CTA exits
       ptx::wait_bounded(bar(KV_FULL), 0, W, false);
-      for (int i = q_issued > 2 ? q_issued - 2 : 0; i < q_issued; ++i)
-        ptx::wait_bounded(bar(QFULL0 + (i & 1)), (i >> 1) & 1, W, false);
+      for (int i = q_issued > kQSt ? q_issued - kQSt : 0; i < q_issued; ++i)
+        ptx::wait_bounded(barm(QFULL0, ring_stage<kQSt>(i)), ring_phase<kQSt>(i), W, false);
       for (int i = do_issued > kDoSt ? do_issued - kDoSt : 0; i < do_issued; ++i)
-        ptx::wait_bounded(bar(DOFULL0 + i % kDoSt), (i / kDoSt) & 1, W, false);
+        ptx::wait_bounded(barm(DOFULL0, ring_stage<kDoSt>(i)), ring_phase<kDoSt>(i), W, false);
     }
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
     // ------------------------------------------------------------ MMA issue
@@ -400,23 +460,41 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     auto mndesc = [&](uint32_t tile, int kk) -> uint64_t {
       return ptx::sdesc_sw128(tile + kk * 2048, Ly::kChunk, 1024);
     };
-    constexpr int kSB = Ly::kSBufs;
     const uint32_t tdP = tm + Ly::kColdP;
-    const uint32_t tdQ = tm + Ly::kColdQ, tdV = tm + Ly::kColdV, tdK = tm + Ly::kColdK;
-    auto tS = [&](int i) -> uint32_t { return tm + (kSB == 2 && (i & 1) ? Ly::kColS1 : Ly::kColS); };
+    const uint32_t tdV = tm + Ly::kColdV, tdK = tm + Ly::kColdK;
     // S^T(i) = K Q(i)^T into buffer i % kSB
     auto issue_S = [&](int i) {
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tS(i), kdesc(sK, kk), kdesc(sQ(i & 1), kk), kIdS, kk > 0);
-      ptx::tc_commit(bar(S_FULL0 + (kSB == 2 ? (i & 1) : 0)));
+      for (int kk = 0; kk < HD / 16; ++kk)
+        ptx::mma_ss(tS(i), kdesc(sK, kk), kdesc(sQ(ring_stage<kQSt>(i)), kk), kIdS, kk > 0);
+      ptx::tc_commit(barm(S_FULL0, (kSB == 2 ? (i & 1) : 0)));
     };
-    // dP^T = V dO^T into the columns that held dQ of the previous block; the
-    // dO stage's dP reader is done at this commit
+    // dP^T = V dO^T; the dO stage's dP reader is done at this commit
     auto issue_dP = [&](int sd) {
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) ptx::mma_ss(tdP, kdesc(sV, kk), kdesc(sdO(sd), kk), kIdS, kk > 0);
       ptx::tc_commit(bar(DP_FULL));
-      ptx::tc_commit(bar(DOEMPTY0 + sd));
+      ptx::tc_commit(barm(DOEMPTY0, sd));
+    };
+    // dK += dS^T Q (the last reader of Q(i): S(i) read it before P(i) existed)
+    auto issue_dK = [&](int i) {
+#pragma unroll
+      for (int kk = 0; kk < kBlk / 16; ++kk)
+        ptx::mma_ss(tdK, kdesc(sdS, kk), mndesc(sQ(ring_stage<kQSt>(i)), kk), kIdKV, (i | kk) != 0);
+      ptx::tc_commit(barm(QEMPTY0, ring_stage<kQSt>(i)));
+    };
+    // dQ = dS K
+    auto issue_dQ = [&](int i) {
+#pragma unroll
+      for (int kk = 0; kk < kBlk / 16; ++kk) ptx::mma_ss(tdQ(i), mndesc(sdS, kk), mndesc(sK, kk), kIdQ, kk > 0);
+      ptx::tc_commit(barm(DQ_FULL0, (kSB == 2 ? ((i + 1) & 1) : 0)));
+    };
+    // TMEM column of P^T for the 16-query K step kk of dV: with one S buffer
+    // query columns [32g, 32g + 32) of S became P columns [32g, 32g + 16);
+    // with two, compute warp g owned query columns [16g, 16g + 16) and
+    // [64 + 16g, 64 + 16g + 16) and packed them into P columns [16g, 16g + 16)
+    auto p_col = [](int kk) -> uint32_t {
+      return kSB == 2 ? (kk & 3) * 16 + (kk >> 2) * 8 : (kk >> 1) * 32 + (kk & 1) * 8;
     };
 
     bool ok = warp_wait(bar(KV_FULL), 0, W);
@@ -428,35 +506,84 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         __syncwarp();
       }
       for (int i = 0; ok && i < n_iter; ++i) {
-        const int st = i & 1;
-        const int sd = i % kDoSt;
-        const uint32_t ph = i & 1;
-        // dV += P^T dO   (A = P^T from TMEM: the 16-query k-steps 2g, 2g+1
-        // in columns [32g, 32g + 16)) once P(i) is there and dO(i) has landed
-        // (P(i) does not imply dO(i); the other MMA warp's dP(i) waits for it
-        // too).  With two S buffers dV(i-1) is also confirmed here (before
-        // DV_DONE(i) is committed), freeing the buffer S(i+1) goes into.
-        ok = warp_wait2(bar(P_FULL), ph, bar(DOFULL0 + sd), (i / kDoSt) & 1, W) &&
-             (kSB != 2 || i == 0 || warp_wait(bar(DV_DONE), ph ^ 1, W));
-        if (!ok) break;
+        const int sd = ring_stage<kDoSt>(i);
+        const uint32_t qph = ring_phase<kQSt>(i + 1);  // phase of Q(i+1)
+        if constexpr (kSB == 2) {
+          // S^T(i+1) first, into buffer (i+1) % 2 as soon as its last readers
+          // are done: dV(i-1) (P(i-1) in the lower columns) and the drain of
+          // dQ(i-2) (upper columns).  It is then computed while the compute
+          // warps still turn S(i) into P(i).
+          if (i + 1 < n_iter) {
+            ok = (i < 2 ? warp_wait(barm(QFULL0, ring_stage<kQSt>(i + 1)), qph, W)
+                        : warp_wait2(barm(QFULL0, ring_stage<kQSt>(i + 1)), qph, barm(DQ_EMPTY0, ((i + 1) & 1)),
+                                     ((i - 2) >> 1) & 1, W)) &&
+                 (i < 1 || warp_wait(barm(DV_DONE0, ((i - 1) & 1)), ((i - 1) >> 1) & 1, W));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            if (ptx::elect_one()) issue_S(i + 1);
+            __syncwarp();
+          }
+        }
+        // dV += P^T dO   (A = P^T from TMEM) once P(i) is there and dO(i) has
+        // landed (P(i) does not imply dO(i); the other MMA warp's dP(i)
+        // waits for it too)
+        if (!(ok = warp_wait2(bar(P_FULL), i & 1, barm(DOFULL0, sd), ring_phase<kDoSt>(i), W))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
-            ptx::mma_ts(tdV, tS(i) + (kk >> 1) * 32 + (kk & 1) * 8, mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
-          ptx::tc_commit(bar(DV_DONE));
-          ptx::tc_commit(bar(DOEMPTY0 + sd));
+            ptx::mma_ts(tdV, tS(i) + p_col(kk), mndesc(sdO(sd), kk), kIdKV, (i | kk) != 0);
+          ptx::tc_commit(barm(DV_DONE0, (kSB == 2 ? (i & 1) : 0)));
+          ptx::tc_commit(barm(DOEMPTY0, sd));
         }
         __syncwarp();
-        // S^T(i+1) = K Q(i+1)^T once its buffer's last reader is done: dV(i)
-        // with one buffer, dV(i-1) (confirmed above) with two
+        if constexpr (kSB == 1) {
+          // S^T(i+1) = K Q(i+1)^T once dV(i) has read P(i) out of the buffer
+          if (i + 1 < n_iter) {
+            if (!(ok = warp_wait2(barm(QFULL0, ring_stage<kQSt>(i + 1)), qph, bar(DV_DONE0), i & 1, W))) break;
+            ptx::tc_fence_after();
+            if (ptx::elect_one()) issue_S(i + 1);
+            __syncwarp();
+          }
+        }
+      }
+    } else if constexpr (kSB == 2) {
+      // dP(i+1) as soon as the compute warps have read dP(i) out of tensor
+      // memory; dK(i) once dS(i) is in shared memory; dQ(i) once S(i+1) has
+      // been read out of the buffer whose upper columns take it (for the last
+      // block: once the dQ that was there before has been drained).  The
+      // compute warps write dS(i+1) after DS_EMPTY, committed behind dQ(i).
+      if (ok && (ok = warp_wait(bar(DOFULL0), 0, W))) {
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) issue_dP(0);
+        __syncwarp();
+      }
+      for (int i = 0; ok && i < n_iter; ++i) {
         if (i + 1 < n_iter) {
-          ok = kSB == 2 ? warp_wait(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, W)
-                        : warp_wait2(bar(QFULL0 + (st ^ 1)), ((i + 1) >> 1) & 1, bar(DV_DONE), ph, W);
-          if (!ok) break;
+          const int sd1 = ring_stage<kDoSt>(i + 1);
+          if (!(ok = warp_wait2(bar(DP_READ), i & 1, barm(DOFULL0, sd1), ring_phase<kDoSt>(i + 1), W))) break;
           ptx::tc_fence_after();
-          if (ptx::elect_one()) issue_S(i + 1);
+          if (ptx::elect_one()) issue_dP(sd1);
           __syncwarp();
+        }
+        if (!(ok = warp_wait(bar(DS_FULL), i & 1, W))) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) issue_dK(i);
+        __syncwarp();
+        if (i + 1 < n_iter)
+          ok = warp_wait(barm(S_READ0, ((i + 1) & 1)), ((i + 1) >> 1) & 1, W);
+        else if (i >= 2)
+          ok = warp_wait(barm(DQ_EMPTY0, ((i + 1) & 1)), ((i - 2) >> 1) & 1, W);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          issue_dQ(i);
+          ptx::tc_commit(bar(DS_EMPTY));
+        }
+        __syncwarp();
+        if constexpr (kCount) {
+          ++n_exec;
+          n_masked += block_sees_key(q_first + i, k0, prm.N, prm.offset, prm.causal) ? 0u : 1u;
         }
       }
     } else {
@@ -466,32 +593,26 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         __syncwarp();
       }
       for (int i = 0; ok && i < n_iter; ++i) {
-        const int st = i & 1;
         const uint32_t ph = i & 1;
-        // dQ = dS K ;  dK += dS^T Q.  dQ first so the drain starts early.  The
-        // compute warps overwrite dS only after DP_FULL of the next block,
-        // which completes after this dK.  S(i) read Q(i) before P(i) existed,
-        // so dK(i) is its last reader.
+        // dQ first so that its drain starts early.  The compute warps
+        // overwrite dS only after DP_FULL of the next block, which completes
+        // after this dK.
         if (!(ok = warp_wait(bar(DS_FULL), ph, W))) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk) ptx::mma_ss(tdQ, mndesc(sdS, kk), mndesc(sK, kk), kIdQ, kk > 0);
-          ptx::tc_commit(bar(DQ_FULL));
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            ptx::mma_ss(tdK, kdesc(sdS, kk), mndesc(sQ(st), kk), kIdKV, (i | kk) != 0);
-          ptx::tc_commit(bar(QEMPTY0 + st));
+          issue_dQ(i);
+          issue_dK(i);
         }
         __syncwarp();
         if constexpr (kCount) {
           ++n_exec;
           n_masked += block_sees_key(q_first + i, k0, prm.N, prm.offset, prm.causal) ? 0u : 1u;
         }
-        // dP(i+1) once dQ(i) has been drained and dO(i+1) has landed
+        // dP(i+1) once dQ(i) has been drained out of the columns it shares
+        // and dO(i+1) has landed
         if (i + 1 < n_iter) {
-          const int sd1 = (i + 1) % kDoSt;
-          if (!(ok = warp_wait2(bar(DQ_EMPTY), ph, bar(DOFULL0 + sd1), ((i + 1) / kDoSt) & 1, W))) break;
+          const int sd1 = ring_stage<kDoSt>(i + 1);
+          if (!(ok = warp_wait2(bar(DQ_EMPTY0), ph, barm(DOFULL0, sd1), ring_phase<kDoSt>(i + 1), W))) break;
           ptx::tc_fence_after();
           if (ptx::elect_one()) issue_dP(sd1);
           __syncwarp();
@@ -515,9 +636,10 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     // by the TMA unit, staged through this warp's slot of kStagedUnits 2 KB
     // units: the first units straight from the tensor-memory loads, the rest
     // (d > 64) from registers once the first operation has read the slot.
-    // Vector reductions from registers would queue in the sub-partition's
-    // memory pipe ahead of the compute warps' shared-memory traffic (18 %
-    // slower at d = 128, measured).  The compute warps never wait for this.
+    // Vector reductions straight from registers would queue in the
+    // sub-partition's memory pipe ahead of the compute warps' shared-memory
+    // traffic (measured 17 % slower at d = 128 and 4-6 % at d = 64).  The
+    // compute warps never wait for this.
     const int qq = warp & 3;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
     constexpr int kUnitsQ = HD / 16;                      // 16-column units of this lane quarter
@@ -527,7 +649,9 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     const uint32_t slot = sbase + Ly::kStage + qq * (kStagedUnits * 2048);
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
-      if (!(ok = warp_wait(bar(DQ_FULL), i & 1, W))) break;
+      const int db = kSB == 2 ? ((i + 1) & 1) : 0;  // with two S buffers: the buffer holding dQ(i)
+      const uint32_t tQ = tdQ(i) + lane_off;
+      if (!(ok = warp_wait(barm(DQ_FULL0, db), kSB == 2 ? (i >> 1) & 1 : i & 1, W))) break;
       ptx::tc_fence_after();
       float* dst = prm.dq_accum + (det ? kb * prm.slice_elems : 0) +
                    dq_unit_offset(bh, prm.n_tiles, q_first + i, qq, 0, HD);
@@ -537,7 +661,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
 #pragma unroll
       for (int u = 0; u < kStaged; u += 2) {
         uint32_t r[32];
-        ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + u * 16, r);
+        ptx::tmem_ld32(tQ + u * 16, r);
 #pragma unroll
         for (int v = 0; v < 2; ++v)
 #pragma unroll
@@ -547,13 +671,12 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       }
       uint32_t h[kHeld > 0 ? kHeld * 16 : 1];
       if constexpr (kHeld == 4) {
-        ptx::tmem_ld64(tm + Ly::kColdQ + lane_off + kStaged * 16, tm + Ly::kColdQ + lane_off + kStaged * 16 + 32,
-                       *reinterpret_cast<uint32_t(*)[64]>(h));
+        ptx::tmem_ld64(tQ + kStaged * 16, tQ + kStaged * 16 + 32, *reinterpret_cast<uint32_t(*)[64]>(h));
       } else if constexpr (kHeld == 2) {
-        ptx::tmem_ld32(tm + Ly::kColdQ + lane_off + kStaged * 16, *reinterpret_cast<uint32_t(*)[32]>(h));
+        ptx::tmem_ld32(tQ + kStaged * 16, *reinterpret_cast<uint32_t(*)[32]>(h));
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(DQ_EMPTY));  // the columns are free for dP(i+1)
+      ptx::mbar_arrive(barm(DQ_EMPTY0, db));  // the columns are free for dP(i+1) (or S(i+3))
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -599,90 +722,189 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     const bool key_ok = kr < prm.Nk;
     const int kd = kRect ? k0 - prm.offset : k0;  // key k0 + t visible to query q iff q - kd >= t
     const float sl2 = prm.scale * kLog2e;
-    const int c0 = G * 32;                 // query columns [c0, c0 + 32) of S, dP
-    uint32_t pk[16];                       // P for columns c0 .. c0 + 31, bf16 pairs
-
+    uint32_t pk[16];                       // P for this warp's 32 query columns, bf16 pairs
     bool ok = true;
-    for (int i = 0; i < n_iter; ++i) {
-      const int st = i & 1;
-      const uint32_t ph = i & 1;
-      const int q0 = (q_first + i) * kBlk;
-      // ---- P(i)
-      // S(i); L(i) rows
-      if (!(ok = warp_wait2(bar(S_FULL0 + (Ly::kSBufs == 2 ? st : 0)), Ly::kSBufs == 2 ? (i >> 1) & 1 : ph,
-                            bar(QFULL0 + st), (i >> 1) & 1, W)))
-        break;
-      const uint32_t tSi = tm + (Ly::kSBufs == 2 && st ? Ly::kColS1 : Ly::kColS);
-      ptx::tc_fence_after();
-      {
-        uint32_t r[32];
-        ptx::tmem_ld32(tSi + lane_off + c0, r);
-        const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4 + c0 * 4;
-        // key k0 + t is visible to query q0 + col iff col >= t - rel; the
-        // block needs the mask unless every entry passes (rel >= 127).
-        // Square problems: rel = 0 on the diagonal block only.
-        const int rel = kRect ? q0 - kd : 0;
-        const bool diag = prm.causal && (kRect ? rel < kBlk - 1 : q0 == k0);
+    if constexpr (kSB == 1) {
+      // one S buffer (d > 64)
+      const int c0 = G * 32;               // query columns [c0, c0 + 32) of S, dP
+      for (int i = 0; i < n_iter; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = i & 1;
+        const int q0 = (q_first + i) * kBlk;
+        // ---- P(i)
+        // S(i); L(i) rows
+        if (!(ok = warp_wait2(bar(S_FULL0), ph, barm(QFULL0, st), (i >> 1) & 1, W))) break;
+        const uint32_t tSi = tm + Ly::kColS;
+        ptx::tc_fence_after();
+        {
+          uint32_t r[32];
+          ptx::tmem_ld32(tSi + lane_off + c0, r);
+          const uint32_t sLa = sbase + Ly::kL + st * kBlk * 4 + c0 * 4;
+          // key k0 + t is visible to query q0 + col iff col >= t - rel; the
+          // block needs the mask unless every entry passes (rel >= 127).
+          // Square problems: rel = 0 on the diagonal block only.
+          const int rel = kRect ? q0 - kd : 0;
+          const bool diag = prm.causal && (kRect ? rel < kBlk - 1 : q0 == k0);
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 l4 = ptx::ld_shared_f4(sLa + j * 4);
-          float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
-          float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
-          float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
-          float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
-          if (diag) {
-            const int col = c0 + j;
-            const int lim = t - rel;  // masked iff col < lim
-            p0 = col + 0 < lim ? 0.f : p0;
-            p1 = col + 1 < lim ? 0.f : p1;
-            p2 = col + 2 < lim ? 0.f : p2;
-            p3 = col + 3 < lim ? 0.f : p3;
+          for (int j = 0; j < 32; j += 4) {
+            const float4 l4 = ptx::ld_shared_f4(sLa + j * 4);
+            float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
+            float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
+            float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
+            float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
+            if (diag) {
+              const int col = c0 + j;
+              const int lim = t - rel;  // masked iff col < lim
+              p0 = col + 0 < lim ? 0.f : p0;
+              p1 = col + 1 < lim ? 0.f : p1;
+              p2 = col + 2 < lim ? 0.f : p2;
+              p3 = col + 3 < lim ? 0.f : p3;
+            }
+            pk[j / 2] = ptx::pack_bf16x2(p0, p1);
+            pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
           }
-          pk[j / 2] = ptx::pack_bf16x2(p0, p1);
-          pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
-        }
-        if (!key_ok) {
+          if (!key_ok) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) pk[k] = 0u;
+            for (int k = 0; k < 16; ++k) pk[k] = 0u;
+          }
+          // P columns [c0, c0 + 16) lie over this warp's own S columns
+          ptx::tmem_st16(tSi + lane_off + c0, &pk[0]);
+          ptx::tmem_st_wait();
         }
-        // P columns [c0, c0 + 16) lie over this warp's own S columns
-        ptx::tmem_st16(tSi + lane_off + c0, &pk[0]);
-        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(P_FULL));
+        // ---- dS(i).  Written after DP_FULL(i), which completes after dK(i-1),
+        // the last reader of dS(i-1).
+        if (!(ok = warp_wait(bar(DP_FULL), ph, W))) break;
+        ptx::tc_fence_after();
+        {
+          uint32_t r[32];
+          ptx::tmem_ld32(tm + Ly::kColdP + lane_off + c0, r);
+          const uint32_t sDa = sbase + Ly::kD + st * kBlk * 4 + c0 * 4;
+          uint32_t ds[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            // dS = P * (dP - D): the difference in fp32 (dP and D nearly
+            // cancel), then one bf16x2 product with the packed bf16 P
+            const float4 d4 = ptx::ld_shared_f4(sDa + j * 4);
+            const uint32_t g01 = ptx::pack_bf16x2(__uint_as_float(r[j + 0]) - d4.x, __uint_as_float(r[j + 1]) - d4.y);
+            const uint32_t g23 = ptx::pack_bf16x2(__uint_as_float(r[j + 2]) - d4.z, __uint_as_float(r[j + 3]) - d4.w);
+            ds[j / 2] = ptx::mul_bf16x2(pk[j / 2], g01);
+            ds[j / 2 + 1] = ptx::mul_bf16x2(pk[j / 2 + 1], g23);
+          }
+          // row t of dS^T, query columns [c0, c0 + 32): chunk G / 2, 16-byte
+          // pieces 4 * (G % 2) .. +3, 128-byte swizzle (piece XOR row % 8)
+          const uint32_t row = sdS + (G >> 1) * Ly::kChunk + t * 128;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t piece = (uint32_t)((G & 1) * 4 + u);
+            ptx::st_shared_v4(row + ((piece ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1], ds[4 * u + 2],
+                              ds[4 * u + 3]);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(DS_FULL));
       }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(P_FULL));
-      // ---- dS(i).  Written after DP_FULL(i), which completes after dK(i-1),
-      // the last reader of dS(i-1).
-      if (!(ok = warp_wait(bar(DP_FULL), ph, W))) break;
-      ptx::tc_fence_after();
-      {
-        uint32_t r[32];
-        ptx::tmem_ld32(tm + Ly::kColdP + lane_off + c0, r);
-        const uint32_t sDa = sbase + Ly::kD + st * kBlk * 4 + c0 * 4;
-        uint32_t ds[16];
+    } else {
+      // two S buffers (d <= 64)
+      // Query columns of S and dP this warp owns: [cA, cA + 16) and
+      // [cB, cB + 16), so that its P (16 packed columns) goes over its own
+      // first 16 and the upper 64 columns of the buffer are free once S has
+      // been read.  Element j of the 32 is column col(j).
+      const int cA = 16 * G, cB = 64 + 16 * G;
+      auto col = [&](int j) -> int { return j < 16 ? cA + j : cB + (j - 16); };
+      auto ld_cols = [&](uint32_t base, uint32_t (&r)[32]) {
+        ptx::tmem_ld16x2(base + lane_off + cA, base + lane_off + cB, r);
+      };
+
+      for (int i = 0; i < n_iter; ++i) {
+        const int qs = ring_stage<kQSt>(i);  // Q stage (with the L and D rows)
+        const int q0 = (q_first + i) * kBlk;
+        // ---- P(i)
+        // S(i); L(i) rows
+        if (!(ok = warp_wait2(barm(S_FULL0, i & 1), (i >> 1) & 1, barm(QFULL0, qs), ring_phase<kQSt>(i), W))) break;
+        const uint32_t tSi = tS(i);
+        ptx::tc_fence_after();
+        {
+          uint32_t r[32];
+          ld_cols(tSi, r);
+          // the upper columns may take dQ(i-1) now
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(barm(S_READ0, i & 1));
+          // L of columns [cA, cA + 16) and [cB, cB + 16)
+          const uint32_t sLa = sbase + Ly::kL + qs * kBlk * 4 + cA * 4, sLb = sLa + (cB - cA) * 4;
+          // key k0 + t is visible to query q0 + c iff c >= t - rel; the
+          // block needs the mask unless every entry passes (rel >= 127).
+          // Square problems: rel = 0 on the diagonal block only.
+          const int rel = kRect ? q0 - kd : 0;
+          const bool diag = prm.causal && (kRect ? rel < kBlk - 1 : q0 == k0);
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          // dS = P * (dP - D): the difference in fp32 (dP and D nearly
-          // cancel), then one bf16x2 product with the packed bf16 P
-          const float4 d4 = ptx::ld_shared_f4(sDa + j * 4);
-          const uint32_t g01 = ptx::pack_bf16x2(__uint_as_float(r[j + 0]) - d4.x, __uint_as_float(r[j + 1]) - d4.y);
-          const uint32_t g23 = ptx::pack_bf16x2(__uint_as_float(r[j + 2]) - d4.z, __uint_as_float(r[j + 3]) - d4.w);
-          ds[j / 2] = ptx::mul_bf16x2(pk[j / 2], g01);
-          ds[j / 2 + 1] = ptx::mul_bf16x2(pk[j / 2 + 1], g23);
-        }
-        // row t of dS^T, query columns [c0, c0 + 32): chunk G / 2, 16-byte
-        // pieces 4 * (G % 2) .. +3, 128-byte swizzle (piece XOR row % 8)
-        const uint32_t row = sdS + (G >> 1) * Ly::kChunk + t * 128;
+          for (int j = 0; j < 32; j += 4) {
+            const float4 l4 = ptx::ld_shared_f4(j < 16 ? sLa + j * 4 : sLb + (j - 16) * 4);
+            float p0 = ptx::ex2(fmaf(__uint_as_float(r[j + 0]), sl2, -l4.x));
+            float p1 = ptx::ex2(fmaf(__uint_as_float(r[j + 1]), sl2, -l4.y));
+            float p2 = ptx::ex2(fmaf(__uint_as_float(r[j + 2]), sl2, -l4.z));
+            float p3 = ptx::ex2(fmaf(__uint_as_float(r[j + 3]), sl2, -l4.w));
+            if (diag) {
+              const int c = col(j);
+              const int lim = t - rel;  // masked iff c < lim
+              p0 = c + 0 < lim ? 0.f : p0;
+              p1 = c + 1 < lim ? 0.f : p1;
+              p2 = c + 2 < lim ? 0.f : p2;
+              p3 = c + 3 < lim ? 0.f : p3;
+            }
+            pk[j / 2] = ptx::pack_bf16x2(p0, p1);
+            pk[j / 2 + 1] = ptx::pack_bf16x2(p2, p3);
+          }
+          if (!key_ok) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t piece = (uint32_t)((G & 1) * 4 + u);
-          ptx::st_shared_v4(row + ((piece ^ (uint32_t)(t & 7)) << 4), ds[4 * u], ds[4 * u + 1], ds[4 * u + 2],
-                            ds[4 * u + 3]);
+            for (int k = 0; k < 16; ++k) pk[k] = 0u;
+          }
+          // P columns [cA, cA + 16) lie over this warp's own S columns
+          ptx::tmem_st16(tSi + lane_off + cA, &pk[0]);
+          ptx::tmem_st_wait();
         }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(P_FULL));
+        // ---- dS(i).  dP(i) is released as soon as it is in registers, and
+        // dS(i) waits for DS_EMPTY, which follows dK(i-1) and dQ(i-1).
+        if (!(ok = warp_wait(bar(DP_FULL), i & 1, W))) break;
+        ptx::tc_fence_after();
+        {
+          uint32_t r[32];
+          ld_cols(tm + Ly::kColdP, r);
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(DP_READ));
+          const uint32_t sDa = sbase + Ly::kD + qs * kBlk * 4 + cA * 4, sDb = sDa + (cB - cA) * 4;
+          uint32_t ds[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            // dS = P * (dP - D): the difference in fp32 (dP and D nearly
+            // cancel), then one bf16x2 product with the packed bf16 P
+            const float4 d4 = ptx::ld_shared_f4(j < 16 ? sDa + j * 4 : sDb + (j - 16) * 4);
+            const uint32_t g01 = ptx::pack_bf16x2(__uint_as_float(r[j + 0]) - d4.x, __uint_as_float(r[j + 1]) - d4.y);
+            const uint32_t g23 = ptx::pack_bf16x2(__uint_as_float(r[j + 2]) - d4.z, __uint_as_float(r[j + 3]) - d4.w);
+            ds[j / 2] = ptx::mul_bf16x2(pk[j / 2], g01);
+            ds[j / 2 + 1] = ptx::mul_bf16x2(pk[j / 2 + 1], g23);
+          }
+          if (i >= 1 && !(ok = warp_wait(bar(DS_EMPTY), (i - 1) & 1, W))) break;
+          // row t of dS^T: 16-byte pieces (8 query columns) of the 64-column
+          // chunks, 128-byte swizzle (piece XOR row % 8).  ds[4u .. 4u + 3]
+          // holds this warp's columns col(8u) .. +7: chunk u / 2, piece
+          // 2G + u % 2.
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t chunk = (uint32_t)(u >> 1);
+            const uint32_t piece = (uint32_t)(2 * G + (u & 1));
+            ptx::st_shared_v4(sdS + chunk * Ly::kChunk + t * 128 + ((piece ^ (uint32_t)(t & 7)) << 4), ds[4 * u],
+                              ds[4 * u + 1], ds[4 * u + 2], ds[4 * u + 3]);
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(DS_FULL));
       }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(DS_FULL));
     }
     if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
       ptx::tc_fence_after();
