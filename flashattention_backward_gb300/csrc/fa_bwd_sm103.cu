@@ -120,6 +120,7 @@ enum BarId {
   DS_EMPTY,     // two S buffers: dS(i) read by dK(i) and dQ(i)
   DQ_FULL1,
   DQ_EMPTY1,
+  SLOTS_FREE,   // the drain warps' last bulk operations have read their staging slots
   kNumBars
 };
 
@@ -215,35 +216,6 @@ __device__ __forceinline__ bool block_sees_key(int qb, int k0, int N, int offset
 using ptx::warp_wait;
 using ptx::warp_wait2;
 
-// NC fp32 columns of this thread's TMEM lane -> bf16 in global (NC a
-// multiple of 16: 32-column pieces, then a 16-column tail).
-__device__ __forceinline__ void store_cols(const uint32_t* r, int n, __nv_bfloat16* dst, float mul) {
-#pragma unroll
-  for (int u = 0; u < n / 8; ++u) {
-    uint4 v;
-    v.x = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 0]) * mul, __uint_as_float(r[8 * u + 1]) * mul);
-    v.y = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 2]) * mul, __uint_as_float(r[8 * u + 3]) * mul);
-    v.z = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 4]) * mul, __uint_as_float(r[8 * u + 5]) * mul);
-    v.w = ptx::pack_bf16x2(__uint_as_float(r[8 * u + 6]) * mul, __uint_as_float(r[8 * u + 7]) * mul);
-    *reinterpret_cast<uint4*>(dst + u * 8) = v;
-  }
-}
-template <int NC>
-__device__ __forceinline__ void store_row(uint32_t taddr, bool valid, __nv_bfloat16* dst, float mul) {
-  static_assert(NC % 16 == 0, "16-column granularity");
-#pragma unroll
-  for (int c = 0; c < NC / 32; ++c) {
-    uint32_t r[32];
-    ptx::tmem_ld32(taddr + c * 32, r);
-    if (valid) store_cols(r, 32, dst + c * 32, mul);
-  }
-  if constexpr (NC % 32 == 16) {
-    uint32_t r[16];
-    ptx::tmem_ld16(taddr + (NC / 32) * 32, r);
-    if (valid) store_cols(r, 16, dst + (NC / 32) * 32, mul);
-  }
-}
-
 // Bounded wait until *c >= target (acquire, GPU scope), polled by one thread.
 __device__ __forceinline__ bool wait_counter(const int32_t* c, int target, uint64_t limit_ns) {
   const uint64_t t0 = ptx::globaltimer();
@@ -270,7 +242,8 @@ __device__ __forceinline__ bool wait_counter(const int32_t* c, int target, uint6
 // in the MMA warp alone measured 2.6 % slower).
 template <int HD, bool kDet, bool kRect, bool kFused, bool kCount>
 __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                          const CUtensorMap& tmdO, const BwdParams& prm, const int kb, const int bh,
+                                          const CUtensorMap& tmdO, const CUtensorMap& tmdK, const CUtensorMap& tmdV,
+                                          const BwdParams& prm, const int kb, const int bh,
                                           const int32_t* ready, int ready_target, int32_t* done) {
   constexpr int LD = HD <= 64 ? 64 : 128;
   using Ly = Layout<LD>;
@@ -310,6 +283,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     ptx::mbar_init(bar(DS_FULL), kComputeThreads);
     ptx::mbar_init(bar(DS_EMPTY), 1);
     ptx::mbar_init(bar(ACC_FULL), 2);  // one commit from each MMA warp
+    ptx::mbar_init(bar(SLOTS_FREE), kDrainThreads);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -344,7 +318,6 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
   // (every key block has one, the last query sees every key)
   const int q_first = !prm.causal ? 0 : !kRect ? kb : (k0 > prm.offset ? (k0 - prm.offset) / kBlk : 0);
   const int n_iter = prm.n_tiles - q_first;
-  const int64_t khead = (int64_t)b * prm.ksb + (int64_t)h * prm.ksh;
   const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
 
   const uint32_t sK = sbase + Ly::kK, sV = sbase + Ly::kV;
@@ -707,11 +680,19 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         }
       }
     }
+    // The staging slots are free once this warp's operations have read them
+    // (the epilogue stores dK through them).  Their writes to global memory
+    // need not be waited for before the CTA exits (they are complete when the
+    // grid is), except in the single-launch backward, which publishes them.
     if (lane == 0) {
-      ptx::bulk_wait_all();  // this warp's bulk operations are complete
-      if (kFused) asm volatile("fence.proxy.async.global;" ::: "memory");
+      ptx::bulk_wait_read_all();
+      if (kFused) {
+        ptx::bulk_wait_all();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
     }
     __syncwarp();
+    ptx::mbar_arrive(bar(SLOTS_FREE));
   } else {
     // ------------------------------------------------------------ compute
     const int qq = warp & 3;               // TMEM lane quarter
@@ -906,16 +887,58 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         ptx::mbar_arrive(bar(DS_FULL));
       }
     }
-    if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
+    // ---- epilogue: this lane's key row t of dV (warps G = 0, 1) or scale *
+    // dK (G = 2, 3), half the columns each, into shared memory as the
+    // 64-column, 128-byte-swizzled chunks of a TMA box: dV into the dS buffer
+    // (its last readers, dK and dQ of the last block, are done at ACC_FULL),
+    // dK over the dQ staging slots once the drain warps' last operations have
+    // read them.  Two TMA stores then write whole lines (rows past N_k and
+    // columns past d are not written).  Stores from registers, each lane its
+    // own row 16 bytes at a time, took ~6 k cycles per CTA at d = 128.
+    // Every compute warp reaches the named barrier below, also after a wait
+    // ran out (which set the CTA's abort flag): the stores are then skipped.
+    const bool isV = G < 2;
+    if (ok && warp_wait(bar(ACC_FULL), 0, W) && (isV || warp_wait(bar(SLOTS_FREE), 0, W))) {
       ptx::tc_fence_after();
-      constexpr int kHalf = HD / 2;        // warps G = 0, 1 store dV, G = 2, 3 store dK
+      constexpr int kHalf = HD / 2;
       const int cc = (G & 1) * kHalf;
-      if (G < 2)
-        store_row<kHalf>(tm + Ly::kColdV + lane_off + cc, key_ok, prm.dV + khead + (int64_t)kr * prm.ksn + cc, 1.0f);
-      else
-        store_row<kHalf>(tm + Ly::kColdK + lane_off + cc, key_ok, prm.dK + khead + (int64_t)kr * prm.ksn + cc,
-                         prm.scale);
+      const uint32_t src = tm + (isV ? Ly::kColdV : Ly::kColdK) + lane_off + cc;
+      const uint32_t dst = isV ? sdS : sbase + Ly::kStage;
+      const float mul = isV ? 1.f : prm.scale;
+#pragma unroll 1
+      for (int c = 0; c < kHalf; c += 16) {
+        uint32_t v[16];
+        ptx::tmem_ld16(src + c, v);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {  // 8 columns (16 bytes) each
+          const int col = cc + c + 8 * q;
+          const uint32_t piece = (uint32_t)((col & 63) >> 3);
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 2 * e]) * mul, __uint_as_float(v[8 * q + 2 * e + 1]) * mul);
+          ptx::st_shared_v4(dst + (col >> 6) * Ly::kChunk + t * 128 + ((piece ^ (uint32_t)(t & 7)) << 4), w[0], w[1],
+                            w[2], w[3]);
+        }
+      }
+      ptx::fence_proxy_async_smem();
     }
+    ptx::bar_sync(1, kComputeThreads);
+    if (warp == 0 && lane == 0 && !*abort_flag) {
+#pragma unroll
+      for (int c = 0; c < LD / 64; ++c) {
+        ptx::tma_store_4d(&tmdV, sdS + c * Ly::kChunk, c * 64, k0, h, b);
+        ptx::tma_store_4d(&tmdK, sbase + Ly::kStage + c * Ly::kChunk, c * 64, k0, h, b);
+      }
+      ptx::bulk_commit();
+      // shared memory is released at exit: the stores must have read it
+      // (and, in the single-launch backward, be complete)
+      if (kFused)
+        ptx::bulk_wait_all();
+      else
+        ptx::bulk_wait_read_all();
+    }
+    __syncwarp();
   }
 
   if (kFused) __threadfence();  // this thread's reductions and stores before the release
@@ -935,6 +958,7 @@ template <int HD, bool kDet, bool kRect, bool kCount>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                      const BwdParams prm) {
   // work item: key block kb of head (b, h).  Heads are taken in groups of
   // prm.head_group so the CTAs resident at any time share a few heads' Q, dO
@@ -946,8 +970,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int grp = blockIdx.x / (hg * prm.nk_tiles);
   const int gsize = min(hg, bh_total - grp * hg);
   const int r = blockIdx.x - grp * hg * prm.nk_tiles;
-  bwd_block<HD, kDet, kRect, false, kCount>(tmQ, tmK, tmV, tmdO, prm, r / gsize, grp * hg + r % gsize, nullptr, 0,
-                                            nullptr);
+  bwd_block<HD, kDet, kRect, false, kCount>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, prm, r / gsize, grp * hg + r % gsize,
+                                            nullptr, 0, nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -1147,6 +1171,7 @@ template <int HD, bool kDet, bool kRect>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                      const BwdParams prm, const FusedParams fp) {
   using Ly = Layout<(HD <= 64 ? 64 : 128)>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -1160,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Ti = (prm.n_tiles + kTilesPerItem - 1) / kTilesPerItem;  // P and C items per head
   fused_item(ticket, BH, Ti, prm.nk_tiles, role, bh, idx);
   if (role == kItemBwd)
-    bwd_block<HD, kDet, kRect, true, false>(tmQ, tmK, tmV, tmdO, prm, idx, bh, fp.sync + 1 + bh, Ti,
+    bwd_block<HD, kDet, kRect, true, false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, prm, idx, bh, fp.sync + 1 + bh, Ti,
                                      fp.sync + 1 + BH + bh);
   else if (role == kItemPre)
     pre_item<HD>(prm, fp, bh, idx, !kDet);
@@ -1176,7 +1201,7 @@ cudaError_t launch_hd(const fa_problem& p, const CUtensorMap* maps, const BwdPar
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((int64_t)prm.nk_tiles * p.B * p.H));
   bwd_sm103_kernel<HD, kDet, kRect, kCount><<<grid, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3],
-                                                                                prm);
+                                                                                maps[4], maps[5], prm);
   return cudaGetLastError();
 }
 
@@ -1196,7 +1221,7 @@ cudaError_t launch_fused_hd(const CUtensorMap* maps, const BwdParams& prm, const
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
   bwd_fused_kernel<HD, kDet, kRect><<<(unsigned)items, kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3],
-                                                                                prm, fp);
+                                                                                maps[4], maps[5], prm, fp);
   return cudaGetLastError();
 }
 
@@ -1259,9 +1284,10 @@ template <bool kCount>
 cudaError_t launch_bwd(const fa_problem& p, const void* Q, const void* K, const void* V, const void* dO,
                        const float* L, const float* D, float* dq_accum, void* dK, void* dV, int32_t* status,
                        uint64_t wait_ns, cudaStream_t s, unsigned long long* pair_count) {
-  CUtensorMap maps[4];
+  CUtensorMap maps[6];
   if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
-      !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false))
+      !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false) ||
+      !make_bf16_tile_map(&maps[4], dK, p, true) || !make_bf16_tile_map(&maps[5], dV, p, true))
     return cudaErrorInvalidValue;
   BwdParams prm = bwd_params(p, L, D, dq_accum, dK, dV, status, wait_ns);
   prm.pair_count = pair_count;
@@ -1302,9 +1328,10 @@ cudaError_t launch_bwd_fused_sm103(const fa_problem& p, const void* Q, const voi
                                    void* dK, void* dV, int32_t* status, uint64_t wait_ns, cudaStream_t s) {
   const int64_t items = fused_items(p);
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
-  CUtensorMap maps[4];
+  CUtensorMap maps[6];
   if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map(&maps[1], K, p, true) ||
-      !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false))
+      !make_bf16_tile_map(&maps[2], V, p, true) || !make_bf16_tile_map(&maps[3], dO, p, false) ||
+      !make_bf16_tile_map(&maps[4], dK, p, true) || !make_bf16_tile_map(&maps[5], dV, p, true))
     return cudaErrorInvalidValue;
   const BwdParams prm = bwd_params(p, L, D, dq_accum, dK, dV, status, wait_ns);
   FusedParams fp;
