@@ -146,7 +146,8 @@ constexpr int fwd_ld(int hd) { return hd <= 64 ? 64 : (hd <= 128 ? 128 : 256); }
 template <int HD>
 __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
     fwd_sm103_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const FwdParams prm) {
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const FwdParams prm) {
   constexpr int LD = fwd_ld(HD);
   using Ly = FwdLayout<LD>;
   constexpr int BK = Ly::BK;       // keys per block
@@ -202,7 +203,6 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
     const int hi = min(q0 + kBlk - 1, prm.N - 1) + prm.offset;
     n_blk = hi < 0 ? 0 : min(nk_blocks, hi / BK + 1);
   }
-  const int64_t head = (int64_t)b * prm.sb + (int64_t)h * prm.sh;
   const ptx::Waiter W{abort_flag, prm.status, prm.wait_ns};
   const uint32_t sQ = sbase + Ly::kQ;
   auto sK = [&](int st) -> uint32_t { return sbase + Ly::kK + st * Ly::kKVTile; };
@@ -438,7 +438,11 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(P_FULL0 + sb));
     }
-    // epilogue: O / l and L
+    // epilogue: O / l and L.  O goes into the Q tile (dead once the last S
+    // has been computed, which O += P V of the last block implies) as the
+    // 64-column, 128-byte-swizzled chunks of a TMA box, and one TMA store
+    // writes it (whole lines; rows past N are not written).  Stores from
+    // registers, each lane its own row 16 bytes at a time, are uncoalesced.
     if (ok) {
       xchg[G * kBlk + t] = l_part;
       named_bar_sync(1 + qq, 32 * NG);
@@ -453,35 +457,39 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
         const bool empty = !(l > 0.f);
         const float inv = empty ? 0.f : 1.f / l;
         constexpr int kOC = HD / 2;
-        __nv_bfloat16* orow = prm.O + head + (int64_t)qrow * prm.sn + G * kOC;
-        // 32-column pieces, then a 16-column tail (d = 32, 96)
-        auto put = [&](const uint32_t* o, int n, int c) {
-#pragma unroll
-          for (int u = 0; u < n / 8; ++u) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (!empty) {
-              v.x = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv, __uint_as_float(o[8 * u + 1]) * inv);
-              v.y = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv, __uint_as_float(o[8 * u + 3]) * inv);
-              v.z = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv, __uint_as_float(o[8 * u + 5]) * inv);
-              v.w = ptx::pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv, __uint_as_float(o[8 * u + 7]) * inv);
-            }
-            *reinterpret_cast<uint4*>(orow + c + 8 * u) = v;
-          }
-        };
-#pragma unroll
-        for (int c = 0; c + 32 <= kOC; c += 32) {
-          uint32_t o[32];
-          if (n_blk > 0) ptx::tmem_ld32(tm + Ly::kColO + lane_off + G * kOC + c, o);
-          if (qrow < prm.N) put(o, 32, c);
-        }
-        if constexpr (kOC % 32 == 16) {
+#pragma unroll 1
+        for (int c = 0; c < kOC; c += 16) {
           uint32_t o[16];
-          if (n_blk > 0) ptx::tmem_ld16(tm + Ly::kColO + lane_off + G * kOC + kOC - 16, o);
-          if (qrow < prm.N) put(o, 16, kOC - 16);
+          if (n_blk > 0) ptx::tmem_ld16(tm + Ly::kColO + lane_off + G * kOC + c, o);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {  // 8 columns (16 bytes) each
+            const int col = G * kOC + c + 8 * q;
+            const uint32_t piece = (uint32_t)((col & 63) >> 3);
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = empty ? 0u : ptx::pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv,
+                                                  __uint_as_float(o[8 * q + 2 * e + 1]) * inv);
+            ptx::st_shared_v4(sQ + (col >> 6) * Ly::kQChunk + t * 128 + ((piece ^ (uint32_t)(t & 7)) << 4), w[0],
+                              w[1], w[2], w[3]);
+          }
         }
+        ptx::fence_proxy_async_smem();
         if (G == 0 && qrow < prm.N)
           prm.L[(int64_t)bh * prm.N + qrow] = empty ? INFINITY : (m_run + log2f(l)) * kLn2;
       }
+    }
+    // every O warp reaches this barrier (also after a wait ran out, which
+    // set the CTA's abort flag: the store is then skipped)
+    if (G < 2) {
+      named_bar_sync(5, 32 * 8);
+      if (warp == 0 && lane == 0 && !*abort_flag) {
+#pragma unroll
+        for (int c = 0; c < LD / 64; ++c) ptx::tma_store_4d(&tmO, sQ + c * Ly::kQChunk, c * 64, q0, h, b);
+        ptx::bulk_commit();
+        ptx::bulk_wait_read_all();  // shared memory is released at exit
+      }
+      __syncwarp();
     }
   }
 
@@ -499,7 +507,7 @@ cudaError_t launch_fwd_hd(const fa_problem& p, const CUtensorMap* maps, const Fw
   cudaError_t e = cudaFuncSetAttribute(fwd_sm103_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((int64_t)prm.n_tiles * p.B * p.H));
-  fwd_sm103_kernel<HD><<<grid, Ly::kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], prm);
+  fwd_sm103_kernel<HD><<<grid, Ly::kThreads, Ly::kBytes, s>>>(maps[0], maps[1], maps[2], maps[3], prm);
   return cudaGetLastError();
 }
 
@@ -507,10 +515,10 @@ cudaError_t launch_fwd_hd(const fa_problem& p, const CUtensorMap* maps, const Fw
 
 cudaError_t launch_fwd_sm103(const fa_problem& p, const void* Q, const void* K, const void* V, void* O, float* L,
                              int32_t* status, uint64_t wait_ns, cudaStream_t s) {
-  CUtensorMap maps[3];
+  CUtensorMap maps[4];
   const int bk = p.d == 256 ? 64 : kBlk;  // key block rows
   if (!make_bf16_tile_map(&maps[0], Q, p, false) || !make_bf16_tile_map_rows(&maps[1], K, p, true, bk) ||
-      !make_bf16_tile_map_rows(&maps[2], V, p, true, bk))
+      !make_bf16_tile_map_rows(&maps[2], V, p, true, bk) || !make_bf16_tile_map(&maps[3], O, p, false))
     return cudaErrorInvalidValue;
   FwdParams prm;
   prm.O = (__nv_bfloat16*)O;
