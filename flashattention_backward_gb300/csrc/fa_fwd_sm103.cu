@@ -140,6 +140,10 @@ using ptx::warp_wait;
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive on named barrier `id` without waiting.
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 constexpr int fwd_ld(int hd) { return hd <= 64 ? 64 : (hd <= 128 ? 128 : 256); }
 
@@ -352,11 +356,19 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
     float* xchg = reinterpret_cast<float*>(smem + Ly::kX);
     float m_run = -INFINITY;               // exponent base (log2 units)
     float l_part = 0.f;                    // this warp's part of the row sum
+    // Every softmax warp meets its lane quarter's named barrier n_blk + 1
+    // times (once per block, once in the epilogue).  A warp whose wait runs
+    // out leaves the loop and makes up the rest with non-blocking arrivals,
+    // so that no warp of its quarter blocks there for good.
+    int met = n_blk + 1;                   // barrier meetings done when leaving the loop early
     bool ok = true;
     for (int j = 0; j < n_blk; ++j) {
       const int sb = j % kSBufs;       // TMEM buffer of S_j / P_j
       const uint32_t tS = tm + sb * BK;
-      if (!(ok = warp_wait(bar(S_FULL0 + sb), (j / kSBufs) & 1, W))) break;
+      if (!(ok = warp_wait(bar(S_FULL0 + sb), (j / kSBufs) & 1, W))) {
+        met = j;
+        break;
+      }
       ptx::tc_fence_after();
       uint32_t r[KC];
       if constexpr (KC == 64)
@@ -407,7 +419,10 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
         const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.f;
         l_part *= alpha;
         if (G < 2) {
-          if (!(ok = warp_wait(bar(O_DONE0 + (j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, W))) break;
+          if (!(ok = warp_wait(bar(O_DONE0 + (j - 1) % kSBufs), ((j - 1) / kSBufs) & 1, W))) {
+            met = j + 1;
+            break;
+          }
           ptx::tc_fence_after();
           constexpr int kOC = HD / 2;  // this warp's O columns, in 16-column pieces
 #pragma unroll
@@ -438,6 +453,7 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(P_FULL0 + sb));
     }
+    for (int k = met; k < n_blk + 1; ++k) named_bar_arrive(1 + qq, 32 * NG);
     // epilogue: O / l and L.  O goes into the Q tile (dead once the last S
     // has been computed, which O += P V of the last block implies) as the
     // 64-column, 128-byte-swizzled chunks of a TMA box, and one TMA store
