@@ -14,7 +14,8 @@
 // still work on P_{b-1} and P_{b-2}; S_b and O += P_b V_b are issued by two
 // warps, each waiting only for its own inputs.
 // K lives in three shared-memory stages (two at d = 256), each freed as soon
-// as its S block is done; V in two, each freed when its O += P V is done.
+// as its S block is done; V in three at d = 96, 128 (two otherwise), each
+// freed when its O += P V is done.
 // At d = 256 the 64-key blocks keep a 64 KB Q tile and two stages each of K
 // and V (32 KB a tile) inside shared memory, and O takes tensor-memory
 // columns 256-511 beside three 64-column S buffers.
@@ -57,7 +58,7 @@ namespace {
 
 constexpr int kBlk = 128;
 constexpr int kKStages = 3;  // K tiles in shared memory (at most; two at d = 256)
-constexpr int kVStages = 2;  // V tiles in shared memory
+constexpr int kVStages = 3;  // V tiles in shared memory (at most; two at d = 256)
 constexpr int kSBufs = 3;    // S/P buffers in TMEM
 constexpr int kHeadGroup = 4;  // heads whose query blocks interleave in the grid order
 constexpr float kLog2e = 1.4426950408889634f;
@@ -103,15 +104,22 @@ struct FwdLayout {
   static constexpr int kMmaPV = kSplitMma ? kSmWarps + 3 : kMma;  // issues the O += P V products
   static constexpr int kThreads = 32 * (kSmWarps + (kSplitMma ? 4 : 3));
   static constexpr int BK = LD == 256 ? 64 : 128;       // keys per block
+  // Three stages each of K and V at d = 96, 128: with two V stages V_b waited
+  // for O += P_{b-2} V_{b-2}, and with two K stages K_b for S_{b-2}, so a TMA
+  // load sat in the per-block chain (measured: 1×32×8192×128 causal 1314-1320
+  // TFLOPS against 1158-1162 with two V stages, 930 with two K stages).  At
+  // d <= 64 a third V stage would leave room for one CTA per SM instead of
+  // two (measured slower); d = 256 has room for two of each.
   static constexpr int kKSt = LD == 256 ? 2 : kKStages;  // K stages
+  static constexpr int kVSt = LD == 128 ? kVStages : 2;  // V stages
   static constexpr int kQChunk = kBlk * 128;            // 128 rows x 64 columns
   static constexpr int kKVChunk = BK * 128;             // BK rows x 64 columns
   static constexpr int kQTile = kBlk * LD * 2;
   static constexpr int kKVTile = BK * LD * 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQTile;                // kKSt tiles
-  static constexpr int kV = kK + kKSt * kKVTile;        // kVStages tiles
-  static constexpr int kX = kV + kVStages * kKVTile;    // row-sum exchange: [kGroups][128] fp32
+  static constexpr int kV = kK + kKSt * kKVTile;        // kVSt tiles
+  static constexpr int kX = kV + kVSt * kKVTile;        // row-sum exchange: [kGroups][128] fp32
   static constexpr int kBar = kX + kGroups * kBlk * 4;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kBytes = kMisc + 16;
@@ -222,7 +230,7 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
     // barriers per block.  Forwarding block b-1 after issuing block b keeps
     // one copy in flight while the previous one is confirmed.
     const bool isK = warp == Ly::kProdK;
-    const int nst = isK ? kKSt : kVStages;
+    const int nst = isK ? kKSt : Ly::kVSt;
     const int full0 = isK ? K_FULL0 : V_FULL0, empty0 = isK ? K_EMPTY0 : V_EMPTY0;
     const CUtensorMap* map = isK ? &tmK : &tmV;
     auto forward = [&](int j) -> bool {
@@ -311,7 +319,7 @@ __global__ void __launch_bounds__(FwdLayout<fwd_ld(HD)>::kThreads, 1)
     // O += P_j V_j  (A = P_j from TMEM: the 16-key steps of softmax warp g
     // of a lane quarter in columns [g KC, g KC + KC/2)) once P_j and V_j are there
     auto issue_PV = [&](int j) -> bool {
-      const int sb = j % kSBufs, vs = j % kVStages;
+      const int sb = j % kSBufs, vs = j % Ly::kVSt;
       if (!warp_wait(bar(P_FULL0 + sb), (j / kSBufs) & 1, W)) return false;  // P_j and V_j
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
