@@ -68,6 +68,30 @@ def test_convert_undoes_the_documented_layout(dtype, d, N):
     assert torch.equal(dq.cpu(), expect)  # bitwise: same fp32 product, same RNE cast
 
 
+@pytest.mark.parametrize("dtype,d,N", [(torch.bfloat16, 128, 300), (torch.bfloat16, 64, 129),
+                                       (torch.bfloat16, 32, 77), (torch.float32, 16, 48),
+                                       (torch.float32, 128, 130)])
+def test_convert_to_an_output_off_the_32_byte_grid(dtype, d, N):
+    """dQ starting 16 bytes past a 32-byte boundary takes the 128-bit store
+    path; the result is the same, and the guard elements on both sides stay."""
+    B, H = 2, 2
+    q = torch.empty(B, H, N, d, dtype=dtype)
+    p = fa.problem_for(q, 0.37, False)
+    gen = torch.Generator().manual_seed(16)
+    acc = torch.randn(fa.fa_dq_accum_elems(p), generator=gen)
+    shift = 16 // q.element_size()
+    n = B * H * N * d
+    buf = torch.full((n + 2 * shift,), -7.0, dtype=dtype, device=DEV)
+    dq = buf[shift:shift + n].view(B, H, N, d)
+    assert dq.data_ptr() % 32 == 16
+    fa.fa_convert_dq(p, acc.to(DEV), dq)
+    torch.cuda.synchronize()
+    idx = _accum_index(B, H, N, d)
+    expect = (torch.from_numpy(acc.numpy()[idx]) * torch.tensor(0.37, dtype=torch.float32)).to(dtype)
+    assert torch.equal(dq.cpu(), expect)
+    assert bool((buf[:shift] == -7.0).all()) and bool((buf[shift + n:] == -7.0).all())
+
+
 def test_forward_four_numbers_across_a_tile_boundary():
     """The write-up's four-number example spread over two 64-key tiles:
     scores 0 then 10, values 0 then 1 -> 0.9999546 (not the 0.5 of a naive
