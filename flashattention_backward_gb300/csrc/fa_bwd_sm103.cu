@@ -120,7 +120,6 @@ enum BarId {
   DS_EMPTY,     // two S buffers: dS(i) read by dK(i) and dQ(i)
   DQ_FULL1,
   DQ_EMPTY1,
-  SLOTS_FREE,   // the drain warps' last bulk operations have read their staging slots
   kNumBars
 };
 
@@ -283,7 +282,6 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     ptx::mbar_init(bar(DS_FULL), kComputeThreads);
     ptx::mbar_init(bar(DS_EMPTY), 1);
     ptx::mbar_init(bar(ACC_FULL), 2);  // one commit from each MMA warp
-    ptx::mbar_init(bar(SLOTS_FREE), kDrainThreads);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -680,10 +678,10 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
         }
       }
     }
-    // The staging slots are free once this warp's operations have read them
-    // (the epilogue stores dK through them).  Their writes to global memory
-    // need not be waited for before the CTA exits (they are complete when the
-    // grid is), except in the single-launch backward, which publishes them.
+    // Shared memory is released at exit, so this warp's last operations must
+    // have read their staging slots.  Their writes to global memory need not
+    // be waited for (they are complete when the grid is), except in the
+    // single-launch backward, which publishes them.
     if (lane == 0) {
       ptx::bulk_wait_read_all();
       if (kFused) {
@@ -692,7 +690,6 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
       }
     }
     __syncwarp();
-    ptx::mbar_arrive(bar(SLOTS_FREE));
   } else {
     // ------------------------------------------------------------ compute
     const int qq = warp & 3;               // TMEM lane quarter
@@ -889,21 +886,22 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
     }
     // ---- epilogue: this lane's key row t of dV (warps G = 0, 1) or scale *
     // dK (G = 2, 3), half the columns each, into shared memory as the
-    // 64-column, 128-byte-swizzled chunks of a TMA box: dV into the dS buffer
-    // (its last readers, dK and dQ of the last block, are done at ACC_FULL),
-    // dK over the dQ staging slots once the drain warps' last operations have
-    // read them.  Two TMA stores then write whole lines (rows past N_k and
-    // columns past d are not written).  Stores from registers, each lane its
-    // own row 16 bytes at a time, took ~6 k cycles per CTA at d = 128.
+    // 64-column, 128-byte-swizzled chunks of a TMA box: dV into the dS buffer,
+    // dK into the first Q stage (their last readers, dK and dQ of the last
+    // block, are done at ACC_FULL, and no Q load is left in flight).  Two TMA
+    // stores then write whole lines (rows past N_k and columns past d are not
+    // written).  Stores from registers, each lane its own row 16 bytes at a
+    // time, took ~6 k cycles per CTA at d = 128; staging dK over the dQ
+    // staging slots, which made it wait for the last dQ drain, cost 0.5-1.3 %.
     // Every compute warp reaches the named barrier below, also after a wait
     // ran out (which set the CTA's abort flag): the stores are then skipped.
     const bool isV = G < 2;
-    if (ok && warp_wait(bar(ACC_FULL), 0, W) && (isV || warp_wait(bar(SLOTS_FREE), 0, W))) {
+    if (ok && warp_wait(bar(ACC_FULL), 0, W)) {
       ptx::tc_fence_after();
       constexpr int kHalf = HD / 2;
       const int cc = (G & 1) * kHalf;
       const uint32_t src = tm + (isV ? Ly::kColdV : Ly::kColdK) + lane_off + cc;
-      const uint32_t dst = isV ? sdS : sbase + Ly::kStage;
+      const uint32_t dst = isV ? sdS : sQ(0);
       const float mul = isV ? 1.f : prm.scale;
 #pragma unroll 1
       for (int c = 0; c < kHalf; c += 16) {
@@ -928,7 +926,7 @@ __device__ __forceinline__ void bwd_block(const CUtensorMap& tmQ, const CUtensor
 #pragma unroll
       for (int c = 0; c < LD / 64; ++c) {
         ptx::tma_store_4d(&tmdV, sdS + c * Ly::kChunk, c * 64, k0, h, b);
-        ptx::tma_store_4d(&tmdK, sbase + Ly::kStage + c * Ly::kChunk, c * 64, k0, h, b);
+        ptx::tma_store_4d(&tmdK, sQ(0) + c * Ly::kChunk, c * 64, k0, h, b);
       }
       ptx::bulk_commit();
       // shared memory is released at exit: the stores must have read it
