@@ -82,3 +82,17 @@ def test_traffic_record_requires_current_kernel_source(tmp_path, monkeypatch):
         assert bench.recorded_traffic(w.with_(name=other)) is None
         rec.write_text(f"kernel_sha256 0000\nbytes_per_launch_{wname} 1234\n")
         assert bench.recorded_traffic(w) is None
+
+
+def test_committed_traffic_records_match_the_kernel_sources():
+    """The committed ncu DRAM figures were taken on the kernels as they are now:
+    each record's hash is that of its kernel source, and it has a figure for
+    the workloads bench.py reports it on."""
+    from fa_inputs import workload
+
+    for wname in ("causal", "long", "hd256"):
+        w = workload(wname)
+        traffic = bench.recorded_traffic(w)
+        assert traffic is not None and traffic > 0, wname
+        # at least the compulsory bytes: Q, K, V, dO read and dK, dV written once (bf16)
+        assert traffic >= 6 * w.B * w.H * w.N * w.d * 2 * 0.9, wname
