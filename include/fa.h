@@ -183,7 +183,10 @@ fa_status fa_bwd_tile_pair_count(const fa_problem* p, const void* Q, const void*
 
 /* dQ = dtype(scale * dQ_accum) (ch.16 §16.3: the convert kernel applies the
  * softmax scale and casts; with FA_FLAG_DETERMINISTIC it first sums the key
- * blocks' slices in increasing order).  Reads dQ_accum, writes dQ. */
+ * blocks' slices in increasing order).  Reads dQ_accum, writes dQ.  When dQ
+ * and its byte strides are multiples of 32 bytes the kernel writes each
+ * 16-column piece of a row with one 256-bit store, else with 128-bit stores;
+ * the values written are the same. */
 fa_status fa_convert_dq(const fa_problem* p, const float* dQ_accum, void* dQ, void* stream);
 
 /* The three backward calls in order: preprocess, bwd, convert. */
